@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""K16/V8 paged decode benchmark (one JSON line on stdout).
+
+A step is one decode layer-step of the whole hot path: kv_append of each
+sequence's new token (FP16 K + E4M3 V), split-KV paged decode attention, and
+the LSE merge, on the Phi-4-shaped workload (40 query / 10 KV heads, d 128,
+16-token pages).  Default workload: decode 1K/batch 32; `--workload 8k`
+selects 8K/batch 16.  The KV pool is replicated so that consecutive steps
+read different copies (the rotation spans >= 4x the L2 size), which keeps the
+timed reads coming from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload (the path has no exchange step); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "K16/V8 paged decode attention: KV GB/s vs HBM peak; µs per layer-step"
+L2_BYTES = 129 * 10 ** 6
+
+
+# ---- multi-process plumbing (replicas only) ---------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(local_ms: float, local_units: float, group=None):
+    """Max step time and summed units over ranks (plain values at N = 1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_ms, local_units
+    backend = dist.get_backend(group)
+    devc = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=devc)
+    u = torch.tensor([local_units], dtype=torch.float64, device=devc)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---- environment records ----------------------------------------------------------
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v
+                          and "Not" not in v})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def traffic_from_profiles(kernel_src: str):
+    """DRAM bytes per launch of the decode split kernel from the committed ncu
+    summary, or None when the kernel source changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "decode_split_1k_b32.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    m_tr = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
+    if not m_src or not m_tr:
+        return None
+    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return float(m_tr.group(1)) if cur == m_src.group(1) else None
+
+
+# ---- the decode workload on the GPU ---------------------------------------------
+
+def kv_bytes(w) -> int:
+    return int(w.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 3
+
+
+class DecodeBench:
+    """Device state for timed decode steps over `replicas` copies of the pool."""
+
+    def __init__(self, w, device, split_chunk=512, replicas=None):
+        import torch
+        from fp8_paged_kv_append_gb300 import k16v8 as K
+        self.K, self.torch, self.w, self.dev = K, torch, w, device
+        self.chunk = split_chunk
+        pool_bytes = w.num_pages * w.num_kv_heads * 16 * w.head_dim * 3
+        self.R = replicas or max(1, -(-4 * L2_BYTES // pool_bytes))
+        P = w.num_pages
+        self.P = P
+        B, hq, d = w.q.shape
+        td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.kc = torch.empty((self.R * P, w.num_kv_heads, 16, d), dtype=torch.float16,
+                              device=device)
+        self.vc = torch.empty((self.R * P, w.num_kv_heads, 16, d), dtype=torch.uint8,
+                              device=device)
+        self.v_scale = td(w.v_scale)
+        k_all, v_all = td(w.k_tok), td(w.v_tok)
+        self.bt, self.slots_new = [], []
+        for r in range(self.R):
+            K.k16v8_kv_append(k_all, v_all, td(w.slot_mapping + r * P * 16), self.v_scale,
+                              self.kc, self.vc)
+            self.bt.append(td(w.block_table + r * P))
+            self.slots_new.append(td(w.slot_mapping[w.new_rows] + r * P * 16))
+        del k_all, v_all
+        self.k_new = td(w.k_tok[w.new_rows])
+        self.v_new = td(w.v_tok[w.new_rows])
+        self.q = td(w.q)
+        self.seq_lens = td(w.seq_lens)
+        self.max_len = int(w.seq_lens.max())
+        self.ws = torch.empty(K.k16v8_decode_workspace_size(B, hq, d, self.max_len, self.chunk),
+                              dtype=torch.uint8, device=device)
+        self.po, self.pl = K.workspace_views(self.ws, B, hq, d, self.max_len, self.chunk)
+        self.out = torch.empty((B, hq, d), dtype=torch.float16, device=device)
+        self.lse = torch.empty((B, hq), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize(device)
+
+    def step(self, i, ev=None):
+        K, r = self.K, i % self.R
+        if ev:
+            ev[0].record()
+        K.k16v8_kv_append(self.k_new, self.v_new, self.slots_new[r], self.v_scale, self.kc,
+                          self.vc, self.err)
+        if ev:
+            ev[1].record()
+        K.k16v8_paged_decode_split(self.q, self.kc, self.vc, self.v_scale, self.bt[r],
+                                   self.seq_lens, self.max_len, self.w.sm_scale, self.chunk,
+                                   self.ws, self.err)
+        if ev:
+            ev[2].record()
+        K.k16v8_merge_states(self.po, self.pl, self.seq_lens, self.chunk, self.out, self.lse)
+        if ev:
+            ev[3].record()
+
+    def run(self, steps, warmup):
+        torch = self.torch
+        for i in range(warmup):
+            self.step(i)
+        torch.cuda.synchronize(self.dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        barrier()
+        torch.cuda.synchronize(self.dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(steps):
+            self.step(warmup + i, evs[i])
+        t1.record()
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        total_ms = t0.elapsed_time(t1)
+        seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]),
+                         e[2].elapsed_time(e[3])] for e in evs])
+        if self.K.k16v8_read_device_error(self.err) != 0:
+            raise RuntimeError("device error flag raised during the benchmark")
+        return total_ms / steps, seg
+
+    def run_e2e(self, steps, warmup):
+        """Same step through host buffers: pinned H2D of the step's inputs, the
+        three launches, D2H of out + lse, all inside the timed region."""
+        torch, K, w = self.torch, self.K, self.w
+        pin = lambda t: t.cpu().pin_memory()
+        h_in = {"q": pin(self.q), "k_new": pin(self.k_new), "v_new": pin(self.v_new),
+                "seq_lens": pin(self.seq_lens)}
+        h_bt = [pin(b) for b in self.bt]
+        h_slots = [pin(s) for s in self.slots_new]
+        h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h_lse = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
+        d_in = {k: torch.empty_like(v, device=self.dev) for k, v in h_in.items()}
+        d_bt = torch.empty_like(self.bt[0])
+        d_slots = torch.empty_like(self.slots_new[0])
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values()) + \
+            h_bt[0].numel() * 4 + h_slots[0].numel() * 8
+        d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+        def one(i):
+            r = i % self.R
+            for k in d_in:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+            d_bt.copy_(h_bt[r], non_blocking=True)
+            d_slots.copy_(h_slots[r], non_blocking=True)
+            K.k16v8_kv_append(d_in["k_new"], d_in["v_new"], d_slots, self.v_scale, self.kc,
+                              self.vc, self.err)
+            K.k16v8_paged_decode_attention(d_in["q"], self.kc, self.vc, self.v_scale, d_bt,
+                                           d_in["seq_lens"], self.max_len, w.sm_scale,
+                                           self.chunk, self.ws, self.out, self.lse, self.err)
+            h_out.copy_(self.out, non_blocking=True)
+            h_lse.copy_(self.lse, non_blocking=True)
+
+        for i in range(warmup):
+            one(i)
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            one(warmup + i)
+        torch.cuda.synchronize(self.dev)
+        dt = (time.perf_counter() - t0) * 1e3 / steps
+        barrier()
+        return dt, h2d, d2h
+
+
+# ---- CPU baseline: the oracle on the host cores -------------------------------------
+
+def oracle_decode_pass(w, okc, ovc, chunk, sample_b, nthreads):
+    """One oracle decode step over sequences sample_b: append the new tokens,
+    split partials, merge.  Returns KV bytes processed."""
+    import oracle
+    rows = w.new_rows[sample_b]
+    oracle.kv_append(w.k_tok[rows], w.v_tok[rows], w.slot_mapping[rows], w.v_scale, okc, ovc)
+    r = oracle.paged_decode(w.q[sample_b], okc, ovc, w.v_scale, w.block_table[sample_b],
+                            w.seq_lens[sample_b], w.sm_scale, split_chunk=chunk,
+                            nthreads=nthreads, want_full=False)
+    nc = -(-w.seq_lens[sample_b] // chunk)
+    oracle.merge(r["partial_o"], r["partial_lse"], nc)
+    return int(w.seq_lens[sample_b].astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 3
+
+
+def run_cpu_baseline(w, chunk, budget_s=12.0):
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    ncores = os.cpu_count() or 1
+    okc = np.zeros((w.num_pages, w.num_kv_heads, 16, w.head_dim), np.float16)
+    ovc = np.zeros((w.num_pages, w.num_kv_heads, 16, w.head_dim), np.uint8)
+    oracle.kv_append(w.k_tok, w.v_tok, w.slot_mapping, w.v_scale, okc, ovc)
+    n = min(w.batch, 4)
+    sample = np.arange(n)
+    t0 = time.perf_counter()
+    bytes_done = 0
+    passes = 0
+    while True:
+        bytes_done += oracle_decode_pass(w, okc, ovc, chunk, sample, ncores)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or passes >= 200:
+            break
+    return {"value": round(bytes_done / el / 1e9, 4), "unit": "GB/s", "cores": ncores,
+            "kind": "oracle",
+            "sample": f"{passes} oracle decode steps (append + split partials + merge) over "
+                      f"sequences 0..{n - 1} of the workload, {el:.1f} s wall"}
+
+
+# ---- main ---------------------------------------------------------------------------
+
+def make_workload(name):
+    from fp8_paged_kv_append_gb300 import workloads
+    if name == "1k":
+        return workloads.decode_1k_b32(), "decode 1K/batch 32", 512
+    if name == "8k":
+        return workloads.decode_8k_b16(), "decode 8K/batch 16", 512
+    raise SystemExit(f"unknown workload {name}")
+
+
+def config_of(w, label, chunk, replicas):
+    return {"workload": f"Phi-4-shaped {label}: one layer, 40 q / 10 KV heads, head_dim 128, "
+                        "16-token pages, FP16 K + E4M3 V",
+            "batch": int(w.batch), "seq_lens": f"{int(w.seq_lens.min())}..{int(w.seq_lens.max())}",
+            "cached_tokens": int(w.seq_lens.sum()), "split_chunk": chunk,
+            "l2": f"{replicas} rotating pool replicas (>= 4x L2) so every step reads HBM"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="1k", choices=["1k", "8k"])
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the secondary 8K/b16 line inside the JSON")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    rank, world, local_rank = dist_env()
+
+    if args.impl == "reference":
+        return main_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    from fp8_paged_kv_append_gb300 import k16v8 as K
+    K.load_library()
+
+    # Replicas only: every rank runs the same seeded workload on its own GPU.
+    w, label, chunk = make_workload(args.workload)
+    bench = DecodeBench(w, device, split_chunk=chunk)
+    clocks = ClockSampler(local_rank).start()
+    ms, seg = bench.run(args.steps, max(args.warmup, 3))
+    clk = clocks.stop()
+    e2e_ms, h2d, d2h = bench.run_e2e(max(10, args.steps // 2), 3)
+    kvb = kv_bytes(w)
+    t_ms, units = aggregate(ms, kvb)
+    te_ms, _ = aggregate(e2e_ms, kvb)
+
+    hbm_peak, _, peak_kind = load_peaks()
+    B, hq, d = w.q.shape
+    split_us = float(np.mean(seg[:, 1])) * 1e3
+    split_bytes = kvb + B * hq * d * 2
+    achieved = split_bytes / (split_us * 1e-6) / 1e9
+    traffic = traffic_from_profiles(os.path.join(ROOT, "fp8_paged_kv_append_gb300", "csrc",
+                                                 "decode.cu"))
+    if traffic is not None and args.workload != "1k":
+        traffic = None
+    line = {
+        "metric": METRIC, "value": round(units / (t_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(t_ms, 5), "us_per_layer_step": round(t_ms * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) Q/K/V, E4M3 V with per-head amax/448 scales)",
+        "config": config_of(w, label, chunk, bench.R),
+        "kernel_us": {"kv_append": round(float(np.mean(seg[:, 0])) * 1e3, 2),
+                      "decode_split": round(split_us, 2),
+                      "merge_states": round(float(np.mean(seg[:, 2])) * 1e3, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": traffic, "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "kernel": "decode_split_kernel",
+                     "algorithmic_bytes_per_launch": split_bytes},
+        "e2e": {"value": round(units / (te_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(te_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = run_cpu_baseline(w, chunk, args.cpu_budget)
+    if not args.no_extra and args.workload == "1k":
+        w8, label8, chunk8 = make_workload("8k")
+        del bench
+        torch.cuda.empty_cache()
+        b8 = DecodeBench(w8, device, split_chunk=chunk8)
+        ms8, seg8 = b8.run(max(10, args.steps // 2), 3)
+        t8, u8 = aggregate(ms8, kv_bytes(w8))
+        s8 = float(np.mean(seg8[:, 1])) * 1e3
+        sb8 = kv_bytes(w8) + w8.batch * w8.num_qo_heads * w8.head_dim * 2
+        line["extra"] = {"decode_8k_b16": {
+            "value": round(u8 / (t8 * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "us_per_layer_step": round(t8 * 1e3, 2),
+            "kernel_us": {"kv_append": round(float(np.mean(seg8[:, 0])) * 1e3, 2),
+                          "decode_split": round(s8, 2),
+                          "merge_states": round(float(np.mean(seg8[:, 2])) * 1e3, 2)},
+            "split_frac_of_hbm_peak": round(sb8 / (s8 * 1e-6) / 1e9 / hbm_peak, 4),
+            "step_frac_of_hbm_peak": round(u8 / (t8 * 1e-3) / 1e9 / hbm_peak, 4),
+            "config": config_of(w8, label8, chunk8, b8.R)}}
+        line["gpu_launches"] += 3 * max(10, args.steps // 2)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main_reference(args, rank, world):
+    """The reference arm: the oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    w, label, chunk = make_workload(args.workload)
+    import oracle
+    okc = np.zeros((w.num_pages, w.num_kv_heads, 16, w.head_dim), np.float16)
+    ovc = np.zeros((w.num_pages, w.num_kv_heads, 16, w.head_dim), np.uint8)
+    oracle.kv_append(w.k_tok, w.v_tok, w.slot_mapping, w.v_scale, okc, ovc)
+    ncores = os.cpu_count() or 1
+    sample = np.arange(min(w.batch, 2))
+    for _ in range(max(args.warmup, 1)):
+        oracle_decode_pass(w, okc, ovc, chunk, sample, ncores)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += oracle_decode_pass(w, okc, ovc, chunk, sample, ncores)
+    el = time.perf_counter() - t0
+    val = round(done / el / 1e9, 4)
+    line = {"metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": config_of(w, label, chunk, 1),
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": ncores, "kind": "oracle",
+                             "sample": f"each step: sequences 0..{len(sample) - 1} of the "
+                                       "workload (append + split partials + merge)"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

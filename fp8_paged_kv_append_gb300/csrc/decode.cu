@@ -1,0 +1,518 @@
+// Paged split-KV decode attention over the K16/V8 cache, and the
+// log-sum-exp merge of its partials.
+//
+// "Phi-4: quality transfer and interrupted throughput studies": the intro
+// gives the format (FP16 K, E4M3 V with per-head scales) and the geometry
+// (40 query heads over 10 KV heads, d = 128); "Matched diagnostic profiles"
+// names the attention and merge kernels.
+//
+// Design (HBM-bound; 3 bytes of cache per element pair):
+//  * One CTA per (split chunk, KV head, sequence); four warps.  The four
+//    query heads of the GQA group share every K/V page read.
+//  * Each warp streams its own pages (pages w, w+4, ... of the chunk)
+//    through a kStages-deep ring in shared memory.  One lane issues two
+//    bulk-async copies per page -- the 4 KB K tile and the 2 KB V tile of one
+//    (page, KV head) are contiguous in the cache layout -- completing on an
+//    mbarrier; no register staging, no address arithmetic per element.
+//  * Q.K: eight lanes own one token (16 dims each, conflict-free 16-byte
+//    shared loads), fp32 FMAs against the pre-scaled query in registers,
+//    then a 3-step reduce-scatter so each lane ends with one (token, head)
+//    score: 4 shuffles per 4 tokens.
+//  * Online softmax in the log2 domain per page (running max / sum).
+//  * P.V: 16 lanes span the 128 dims (8 each), two tokens per step;
+//    E4M3 -> half2 -> fp32 dequant in registers; the per-head value scale is
+//    applied once to the final partial (it factors out of the sum).
+//  * The four warps' states are combined in shared memory; the CTA writes
+//    one fp32 partial row per query head plus its natural-log LSE.
+#include <math.h>
+
+#include "k16v8_device.cuh"
+
+namespace k16v8 {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 4;
+constexpr int kKPageBytes = kPage * kHeadDim * 2;  // 4096
+constexpr int kVPageBytes = kPage * kHeadDim;      // 2048
+constexpr unsigned kFull = 0xffffffffu;
+
+struct __align__(128) WarpRing {
+  uint8_t k[kStages][kKPageBytes];
+  uint8_t v[kStages][kVPageBytes];
+  float p[kPage * kGroup];  // p[token][head] of the page being consumed
+  float alpha[kGroup];      // rescale factor of the running state
+  uint64_t bar[kStages];
+};
+
+static size_t decode_smem_bytes(int split_chunk) {
+  const size_t ids = static_cast<size_t>(split_chunk / kPage) * sizeof(int);
+  return kWarps * sizeof(WarpRing) + ((ids + 15) / 16) * 16;
+}
+
+__device__ __forceinline__ void dot8(const uint4 &raw, const float (&qf)[kGroup][16], int base,
+                                     float (&acc)[kGroup]) {
+  const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h2[i]);
+#pragma unroll
+    for (int h = 0; h < kGroup; ++h) {
+      acc[h] = fmaf(qf[h][base + 2 * i], f.x, acc[h]);
+      acc[h] = fmaf(qf[h][base + 2 * i + 1], f.y, acc[h]);
+    }
+  }
+}
+
+// Sum acc[0..3] over the 8 lanes of a token group; lane j of the group ends
+// with the total of head j >> 1.
+__device__ __forceinline__ float reduce_scatter8(const float (&acc)[kGroup], int j) {
+  const bool up4 = j & 4;
+  const float s0 = up4 ? acc[0] : acc[2];
+  const float s1 = up4 ? acc[1] : acc[3];
+  float k0 = up4 ? acc[2] : acc[0];
+  float k1 = up4 ? acc[3] : acc[1];
+  k0 += __shfl_xor_sync(kFull, s0, 4);
+  k1 += __shfl_xor_sync(kFull, s1, 4);
+  const bool up2 = j & 2;
+  const float snd = up2 ? k0 : k1;
+  float kp = up2 ? k1 : k0;
+  kp += __shfl_xor_sync(kFull, snd, 2);
+  kp += __shfl_xor_sync(kFull, kp, 1);
+  return kp;
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(
+    const __half *__restrict__ q, const __half *__restrict__ k_cache,
+    const uint8_t *__restrict__ v_cache, const float *__restrict__ v_scale,
+    const int32_t *__restrict__ block_table, int32_t maxp, const int32_t *__restrict__ seq_lens,
+    int32_t hq, int32_t hkv, int32_t num_pages, float sm_scale, int32_t chunk,
+    int32_t max_chunks, float *__restrict__ part_o, float *__restrict__ part_lse,
+    int32_t *dev_error) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  WarpRing *rings = reinterpret_cast<WarpRing *>(smem_raw);
+  int *page_ids = reinterpret_cast<int *>(smem_raw + kWarps * sizeof(WarpRing));
+
+  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int L = __ldg(seq_lens + b);
+  const int cap = min(maxp * kPage, max_chunks * chunk);
+  if (L < 0 || L > cap) {
+    if (threadIdx.x == 0 && c == 0 && g == 0) flag_error(dev_error, K16V8_DEVERR_SEQLEN);
+    L = max(0, min(L, cap));
+  }
+  const int start = c * chunk;
+  if (start >= L) return;  // chunk past the end of this sequence
+  const int n_tok = min(chunk, L - start);
+  const int n_pages = (n_tok + kPage - 1) / kPage;
+
+  const int32_t *bt = block_table + static_cast<int64_t>(b) * maxp + start / kPage;
+  for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
+    int pid = __ldg(bt + i);
+    if (pid < 0 || pid >= num_pages) {
+      flag_error(dev_error, K16V8_DEVERR_PAGE);
+      pid = -1;
+    }
+    page_ids[i] = pid;
+  }
+  WarpRing &ring = rings[warp];
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(&ring.bar[s], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int n_my = warp < n_pages ? (n_pages - warp + kWarps - 1) / kWarps : 0;
+  const int64_t head_tile = static_cast<int64_t>(kPage) * kHeadDim;  // elements per (page, head)
+  const uint64_t policy = l2_policy_evict_first();
+  auto issue = [&](int k) {
+    const int s = k % kStages;
+    const int pid = page_ids[warp + k * kWarps];
+    if (pid < 0) {
+      mbar_arrive(&ring.bar[s]);  // nothing to load: complete the phase empty
+      return;
+    }
+    const int64_t tile = (static_cast<int64_t>(pid) * hkv + g) * head_tile;
+    mbar_arrive_expect_tx(&ring.bar[s], kKPageBytes + kVPageBytes);
+    bulk_g2s_evict_first(ring.k[s], k_cache + tile, kKPageBytes, &ring.bar[s], policy);
+    bulk_g2s_evict_first(ring.v[s], v_cache + tile, kVPageBytes, &ring.bar[s], policy);
+  };
+  if (lane == 0)
+    for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
+
+  // Query of the group's 4 heads, pre-multiplied by sm_scale*log2(e).
+  // Lane j of a token group owns dims [8j, 8j+8) and [64+8j, 64+8j+8).
+  const int j = lane & 7;
+  float qf[kGroup][16];
+  {
+    const float qs = sm_scale * kLog2e;
+    const __half *qb = q + (static_cast<int64_t>(b) * hq + g * kGroup) * kHeadDim;
+#pragma unroll
+    for (int h = 0; h < kGroup; ++h) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qb + h * kHeadDim + part * 64 + j * 8));
+        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(h2[i]);
+          qf[h][part * 8 + 2 * i] = f.x * qs;
+          qf[h][part * 8 + 2 * i + 1] = f.y * qs;
+        }
+      }
+    }
+  }
+
+  const int hsel = j >> 1;            // head whose score this lane holds
+  const int d0 = (lane & 15) * 8;     // P.V: this lane's 8 dims
+  const int tpar = lane >> 4;         // P.V: token parity handled
+  float m_run = -INFINITY, l_run = 0.f;
+  float o[kGroup][8];
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+
+  int k = 0;
+  bool ok = true;
+  for (; k < n_my; ++k) {
+    const int s = k % kStages;
+    ok = __all_sync(kFull, mbar_wait_bounded(&ring.bar[s], (k / kStages) & 1));
+    if (!ok) break;
+    const int i = warp + k * kWarps;  // page within the chunk
+    const int valid = min(kPage, n_tok - i * kPage);
+    if (page_ids[i] >= 0) {
+      // ---- scores of 16 tokens x 4 heads ----
+      const uint8_t *kp = ring.k[s];
+      float sc[4];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int t = it * 4 + (lane >> 3);
+        const uint4 a = *reinterpret_cast<const uint4 *>(kp + t * 256 + j * 16);
+        const uint4 bq = *reinterpret_cast<const uint4 *>(kp + t * 256 + 128 + j * 16);
+        float acc[kGroup] = {0.f, 0.f, 0.f, 0.f};
+        dot8(a, qf, 0, acc);
+        dot8(bq, qf, 8, acc);
+        const float v = reduce_scatter8(acc, j);
+        sc[it] = t < valid ? v : -INFINITY;
+      }
+      // ---- online softmax (log2 domain) ----
+      float pm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+      pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 16));
+      const float m_new = fmaxf(m_run, pm);
+      const float alpha = ex2(m_run - m_new);
+      float p[4];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) p[it] = ex2(sc[it] - m_new);
+      l_run = l_run * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+      m_run = m_new;
+      if ((lane & 1) == 0) {
+#pragma unroll
+        for (int it = 0; it < 4; ++it) ring.p[(it * 4 + (lane >> 3)) * kGroup + hsel] = p[it];
+        if (lane < 8) ring.alpha[hsel] = alpha;
+      }
+      __syncwarp();
+      // ---- P.V over this page ----
+      const float4 al = *reinterpret_cast<const float4 *>(ring.alpha);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        o[0][e] *= al.x;
+        o[1][e] *= al.y;
+        o[2][e] *= al.z;
+        o[3][e] *= al.w;
+      }
+      const uint8_t *vp = ring.v[s];
+#pragma unroll
+      for (int tt = 0; tt < kPage / 2; ++tt) {
+        const int t = 2 * tt + tpar;
+        if (t < valid) {
+          const uint2 raw = *reinterpret_cast<const uint2 *>(vp + t * kHeadDim + d0);
+          const float4 pp = *reinterpret_cast<const float4 *>(ring.p + t * kGroup);
+          float vf[8];
+          const uint16_t *pr = reinterpret_cast<const uint16_t *>(&raw);
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2) {
+            const float2 f = __half22float2(e4m3x2_to_half2(pr[i2]));
+            vf[2 * i2] = f.x;
+            vf[2 * i2 + 1] = f.y;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            o[0][e] = fmaf(pp.x, vf[e], o[0][e]);
+            o[1][e] = fmaf(pp.y, vf[e], o[1][e]);
+            o[2][e] = fmaf(pp.z, vf[e], o[2][e]);
+            o[3][e] = fmaf(pp.w, vf[e], o[3][e]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && k + kStages < n_my) {
+      fence_proxy_async();
+      issue(k + kStages);
+    }
+  }
+  if (!ok) {
+    // Give up on this chunk: report, then drain the copies still in flight
+    // (bounded) so none lands after the CTA exits.
+    if (lane == 0) {
+      flag_error(dev_error, K16V8_DEVERR_TIMEOUT);
+      for (int kk = k; kk < min(k + kStages, n_my); ++kk)
+        mbar_wait_bounded(&ring.bar[kk % kStages], (kk / kStages) & 1);
+    }
+    __syncwarp();
+  }
+
+  // ---- combine the token-parity halves and the lanes of each head ----
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(kFull, o[h][e], 16);
+  l_run += __shfl_xor_sync(kFull, l_run, 8);
+  l_run += __shfl_xor_sync(kFull, l_run, 16);
+
+  // ---- combine the four warps in shared memory (ring 0's K tiles) ----
+  __syncthreads();
+  float *wo = reinterpret_cast<float *>(rings[0].k);  // [warp][head][128]
+  float *wm = wo + kWarps * kGroup * kHeadDim;        // [warp][head]
+  float *wl = wm + kWarps * kGroup;
+  if (lane < 8 && (lane & 1) == 0) {
+    wm[warp * kGroup + hsel] = m_run;
+    wl[warp * kGroup + hsel] = l_run;
+  }
+  if (lane < 16) {
+#pragma unroll
+    for (int h = 0; h < kGroup; ++h) {
+      float *dst = wo + (warp * kGroup + h) * kHeadDim + d0;
+      *reinterpret_cast<float4 *>(dst) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+      *reinterpret_cast<float4 *>(dst + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+    }
+  }
+  __syncthreads();
+  {
+    const int h = threadIdx.x >> 5;
+    const int d4 = (threadIdx.x & 31) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kGroup + h]);
+    float Ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = wm[w * kGroup + h];
+      const float sw = mw == -INFINITY ? 0.f : ex2(mw - M);
+      Ls += sw * wl[w * kGroup + h];
+      const float4 ow = *reinterpret_cast<const float4 *>(wo + (w * kGroup + h) * kHeadDim + d4);
+      acc.x += sw * ow.x;
+      acc.y += sw * ow.y;
+      acc.z += sw * ow.z;
+      acc.w += sw * ow.w;
+    }
+    const int64_t row = (static_cast<int64_t>(b) * hq + g * kGroup + h) * max_chunks + c;
+    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lse = -INFINITY;
+    if (Ls > 0.f) {
+      const float inv = __ldg(v_scale + g) / Ls;
+      res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      lse = (M + log2f(Ls)) * kLn2;
+    }
+    *reinterpret_cast<float4 *>(part_o + row * kHeadDim + d4) = res;
+    if ((threadIdx.x & 31) == 0) part_lse[row] = lse;
+  }
+}
+
+// One warp per (sequence, query head); lane owns 4 dims.
+__global__ void __launch_bounds__(128) merge_states_kernel(
+    const float *__restrict__ part_o, const float *__restrict__ part_lse, int32_t rows,
+    int32_t hq, int32_t max_chunks, const int32_t *__restrict__ seq_lens, int32_t chunk,
+    __half *__restrict__ out, float *__restrict__ lse_out) {
+  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= rows) return;
+  const int b = wid / hq;
+  int L = __ldg(seq_lens + b);
+  L = max(0, min(L, max_chunks * chunk));
+  const int nc = (L + chunk - 1) / chunk;
+  const float *pl = part_lse + static_cast<int64_t>(wid) * max_chunks;
+  const float *po = part_o + static_cast<int64_t>(wid) * max_chunks * kHeadDim + lane * 4;
+  float M = -INFINITY;
+  for (int c = lane; c < nc; c += 32) M = fmaxf(M, pl[c]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  float S = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int c = 0; c < nc; ++c) {
+      const float w = ex2((pl[c] - M) * kLog2e);
+      const float4 oc = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(c) * kHeadDim);
+      S += w;
+      acc.x = fmaf(w, oc.x, acc.x);
+      acc.y = fmaf(w, oc.y, acc.y);
+      acc.z = fmaf(w, oc.z, acc.z);
+      acc.w = fmaf(w, oc.w, acc.w);
+    }
+  }
+  float lse = -INFINITY;
+  if (S > 0.f) {
+    const float inv = 1.f / S;
+    acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    lse = M + logf(S);
+  }
+  uint2 st;
+  st.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.x))) |
+         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.y))) << 16);
+  st.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.z))) |
+         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.w))) << 16);
+  *reinterpret_cast<uint2 *>(out + static_cast<int64_t>(wid) * kHeadDim + lane * 4) = st;
+  if (lane == 0 && lse_out) lse_out[wid] = lse;
+}
+
+// ---- host side ------------------------------------------------------------
+
+struct WsLayout {
+  size_t o_off, lse_off, total;
+  int chunks;
+};
+
+static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+static bool ws_layout(int32_t batch, int32_t hq, int32_t d, int32_t max_seq_len, int32_t chunk,
+                      WsLayout *w) {
+  if (batch < 0 || hq <= 0 || d <= 0 || max_seq_len < 0 || chunk <= 0) return false;
+  w->chunks = max(1, (max_seq_len + chunk - 1) / chunk);
+  const size_t rows = static_cast<size_t>(batch) * hq * w->chunks;
+  w->o_off = 0;
+  w->lse_off = align256(rows * d * sizeof(float));
+  w->total = w->lse_off + align256(rows * sizeof(float));
+  return true;
+}
+
+static int32_t set_smem_attr(size_t bytes) {
+  // The attribute is per device; remember the largest size configured.
+  static size_t configured[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return K16V8_ERR_CUDA;
+  if (dev < 64 && configured[dev] >= bytes) return K16V8_OK;
+  if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess)
+    return K16V8_ERR_CUDA;
+  if (dev < 64) configured[dev] = bytes;
+  return K16V8_OK;
+}
+
+static int32_t check_attention_shape(int32_t hq, int32_t hkv, int32_t head_dim) {
+  if (hq <= 0 || hkv <= 0) return K16V8_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || hq != kGroup * hkv) return K16V8_ERR_UNSUPPORTED_SHAPE;
+  return K16V8_OK;
+}
+
+}  // namespace k16v8
+
+using namespace k16v8;
+
+extern "C" size_t k16v8_decode_workspace_size(int32_t batch, int32_t num_qo_heads,
+                                              int32_t head_dim, int32_t max_seq_len,
+                                              int32_t split_chunk) {
+  WsLayout w;
+  if (split_chunk % kPage) return 0;
+  if (!ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w)) return 0;
+  return w.total;
+}
+
+extern "C" int32_t k16v8_decode_workspace_layout(int32_t batch, int32_t num_qo_heads,
+                                                 int32_t head_dim, int32_t max_seq_len,
+                                                 int32_t split_chunk, size_t *partial_o_offset,
+                                                 size_t *partial_lse_offset,
+                                                 int32_t *max_chunks) {
+  WsLayout w;
+  if (split_chunk % kPage || !ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w))
+    return K16V8_ERR_INVALID_ARG;
+  if (partial_o_offset) *partial_o_offset = w.o_off;
+  if (partial_lse_offset) *partial_lse_offset = w.lse_off;
+  if (max_chunks) *max_chunks = w.chunks;
+  return K16V8_OK;
+}
+
+extern "C" int32_t k16v8_paged_decode_split(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t max_seq_len, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, int32_t split_chunk, void *workspace,
+    size_t workspace_bytes, int32_t *dev_error, void *stream) {
+  int32_t st = check_attention_shape(num_qo_heads, num_kv_heads, head_dim);
+  if (st != K16V8_OK) return st;
+  if (batch < 0 || max_seq_len < 0 || num_pages <= 0 || max_pages_per_seq < 0)
+    return K16V8_ERR_INVALID_ARG;
+  if (split_chunk < kPage || split_chunk > K16V8_MAX_SPLIT_CHUNK || split_chunk % kPage)
+    return K16V8_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_pages_per_seq) * kPage < max_seq_len) return K16V8_ERR_INVALID_ARG;
+  if (batch > 65535 || num_kv_heads > 65535) return K16V8_ERR_INVALID_ARG;
+  WsLayout w;
+  if (!ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w))
+    return K16V8_ERR_INVALID_ARG;
+  if (batch == 0) return K16V8_OK;
+  if (!q || !k_cache || !v_cache || !v_scale || !block_table || !seq_lens || !workspace)
+    return K16V8_ERR_INVALID_ARG;
+  if (workspace_bytes < w.total) return K16V8_ERR_WORKSPACE_TOO_SMALL;
+  if (!k16v8_aligned(q, 16) || !k16v8_aligned(k_cache, 16) || !k16v8_aligned(v_cache, 16) ||
+      !k16v8_aligned(workspace, 256) || !k16v8_aligned(block_table, 4) ||
+      !k16v8_aligned(seq_lens, 4) || !k16v8_aligned(v_scale, 4))
+    return K16V8_ERR_INVALID_ARG;
+  if (max_seq_len == 0) return K16V8_OK;  // every sequence empty: nothing to read
+  const size_t smem = decode_smem_bytes(split_chunk);
+  st = set_smem_attr(smem);
+  if (st != K16V8_OK) return st;
+  float *po = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_off);
+  float *pl = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.lse_off);
+  const dim3 grid(w.chunks, num_kv_heads, batch);
+  decode_split_kernel<<<grid, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __half *>(q), static_cast<const __half *>(k_cache), v_cache, v_scale,
+      block_table, max_pages_per_seq, seq_lens, num_qo_heads, num_kv_heads, num_pages, sm_scale,
+      split_chunk, w.chunks, po, pl, dev_error);
+  return k16v8_launch_status();
+}
+
+extern "C" int32_t k16v8_merge_states(const float *partial_o, const float *partial_lse,
+                                      int32_t batch, int32_t num_qo_heads, int32_t max_chunks,
+                                      int32_t head_dim, const int32_t *seq_lens,
+                                      int32_t split_chunk, void *out, float *lse,
+                                      void *stream) {
+  if (batch < 0 || num_qo_heads <= 0 || max_chunks <= 0 || split_chunk <= 0)
+    return K16V8_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return K16V8_ERR_UNSUPPORTED_SHAPE;
+  if (batch == 0) return K16V8_OK;
+  if (!partial_o || !partial_lse || !seq_lens || !out) return K16V8_ERR_INVALID_ARG;
+  if (!k16v8_aligned(partial_o, 16) || !k16v8_aligned(out, 8) || !k16v8_aligned(partial_lse, 4) ||
+      !k16v8_aligned(seq_lens, 4) || (lse && !k16v8_aligned(lse, 4)))
+    return K16V8_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(batch) * num_qo_heads;
+  if (rows > (1LL << 31) - 4) return K16V8_ERR_INVALID_ARG;
+  const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
+  merge_states_kernel<<<blocks, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      partial_o, partial_lse, static_cast<int32_t>(rows), num_qo_heads, max_chunks, seq_lens,
+      split_chunk, static_cast<__half *>(out), lse);
+  return k16v8_launch_status();
+}
+
+extern "C" int32_t k16v8_paged_decode_attention(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t max_seq_len, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, int32_t split_chunk, void *workspace,
+    size_t workspace_bytes, void *out, float *lse, int32_t *dev_error, void *stream) {
+  if (batch > 0 && !out) return K16V8_ERR_INVALID_ARG;
+  int32_t st = k16v8_paged_decode_split(q, k_cache, v_cache, v_scale, block_table,
+                                        max_pages_per_seq, seq_lens, max_seq_len, batch,
+                                        num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale,
+                                        split_chunk, workspace, workspace_bytes, dev_error, stream);
+  if (st != K16V8_OK || batch == 0) return st;
+  WsLayout w;
+  ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w);
+  const uint8_t *base = static_cast<const uint8_t *>(workspace);
+  return k16v8_merge_states(reinterpret_cast<const float *>(base + w.o_off),
+                            reinterpret_cast<const float *>(base + w.lse_off), batch,
+                            num_qo_heads, w.chunks, head_dim, seq_lens, split_chunk, out, lse,
+                            stream);
+}

@@ -1,0 +1,188 @@
+"""Thin Python binding of libk16v8.so (the C ABI in include/k16v8.h).
+
+Argument marshalling only: shapes and strides are read from torch tensors,
+device pointers and the current CUDA stream are passed through ctypes, and
+every status is turned into an exception.  All computation runs in the
+library's CUDA kernels; there is no fallback of any kind -- importing this
+module on a machine without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libk16v8.so")
+
+K16V8_OK = 0
+K16V8_ERR_INVALID_ARG = 1
+K16V8_ERR_UNSUPPORTED_SHAPE = 2
+K16V8_ERR_WORKSPACE_TOO_SMALL = 3
+K16V8_ERR_CUDA = 4
+K16V8_ERR_DEVICE_BOUNDS = 5
+K16V8_F16 = 0
+K16V8_F32 = 1
+DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+PAGE_SIZE = 16
+HEAD_DIM = 128
+
+# Every symbol include/k16v8.h declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_i32, _i64, _sz, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+SIGNATURES = {
+    "k16v8_kv_append": (_i32, [_P, _i64, _P, _i32, _i64, _P, _i32, _P, _P, _P, _i32, _i32,
+                               _i32, _P, _P]),
+    "k16v8_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "k16v8_decode_workspace_layout": (_i32, [_i32, _i32, _i32, _i32, _i32,
+                                             ctypes.POINTER(_sz), ctypes.POINTER(_sz),
+                                             ctypes.POINTER(_i32)]),
+    "k16v8_paged_decode_split": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32, _i32,
+                                        _i32, _i32, _f32, _i32, _P, _sz, _P, _P]),
+    "k16v8_merge_states": (_i32, [_P, _P, _i32, _i32, _i32, _i32, _P, _i32, _P, _P, _P]),
+    "k16v8_paged_decode_attention": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32,
+                                            _i32, _i32, _i32, _f32, _i32, _P, _sz, _P, _P,
+                                            _P, _P]),
+    "k16v8_read_device_error": (_i32, [_P, _P, ctypes.POINTER(_i32)]),
+    "k16v8_status_string": (ctypes.c_char_p, [_i32]),
+}
+
+_lib = None
+
+
+class K16V8Error(RuntimeError):
+    def __init__(self, name: str, status: int):
+        self.status = status
+        super().__init__(f"{name}: {status_string(status)} (status {status})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libk16v8.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libk16v8.so not found at {path}: build it with "
+                "`python -m fp8_paged_kv_append_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().k16v8_status_string(int(status)).decode()
+
+
+k16v8_status_string = status_string
+
+
+def _check(name: str, status: int) -> None:
+    if status != K16V8_OK:
+        raise K16V8Error(name, status)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _row_stride(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError(f"{name} must be [tokens, heads, head_dim] with dense rows")
+    return t.stride(0)
+
+
+# ---- kv_append ---------------------------------------------------------------
+
+def k16v8_kv_append(k, v, slot_mapping, v_scale, k_cache, v_cache, dev_error=None,
+                    stream=None) -> None:
+    """k fp16 [T,Hkv,D]; v fp16/fp32 [T,Hkv,D] (token stride may exceed the
+    row, e.g. a slice of a fused QKV); slot_mapping int64 [T]; v_scale fp32
+    [Hkv]; k_cache fp16 / v_cache uint8 [P,Hkv,16,D]."""
+    T, hkv, d = k.shape
+    vd = {torch.float16: K16V8_F16, torch.float32: K16V8_F32}[v.dtype]
+    st = load_library().k16v8_kv_append(
+        _ptr(k), _row_stride(k, "k"), _ptr(v), vd, _row_stride(v, "v"), _ptr(slot_mapping), T,
+        _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], hkv, d,
+        _ptr(dev_error), _stream(stream))
+    _check("k16v8_kv_append", st)
+
+
+# ---- decode --------------------------------------------------------------------
+
+def k16v8_decode_workspace_size(batch, num_qo_heads, head_dim, max_seq_len, split_chunk) -> int:
+    return int(load_library().k16v8_decode_workspace_size(batch, num_qo_heads, head_dim,
+                                                          max_seq_len, split_chunk))
+
+
+def k16v8_decode_workspace_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk):
+    """(partial_o byte offset, partial_lse byte offset, max_chunks)."""
+    o, l, c = _sz(), _sz(), _i32()
+    st = load_library().k16v8_decode_workspace_layout(
+        batch, num_qo_heads, head_dim, max_seq_len, split_chunk,
+        ctypes.byref(o), ctypes.byref(l), ctypes.byref(c))
+    _check("k16v8_decode_workspace_layout", st)
+    return o.value, l.value, c.value
+
+
+def workspace_views(workspace, batch, num_qo_heads, head_dim, max_seq_len, split_chunk):
+    """fp32 views (partial_o [B,Hq,C,D], partial_lse [B,Hq,C]) of a workspace."""
+    o_off, l_off, C = k16v8_decode_workspace_layout(batch, num_qo_heads, head_dim,
+                                                    max_seq_len, split_chunk)
+    n = batch * num_qo_heads * C
+    po = workspace[o_off:o_off + n * head_dim * 4].view(torch.float32)
+    pl = workspace[l_off:l_off + n * 4].view(torch.float32)
+    return po.view(batch, num_qo_heads, C, head_dim), pl.view(batch, num_qo_heads, C)
+
+
+def k16v8_paged_decode_split(q, k_cache, v_cache, v_scale, block_table, seq_lens, max_seq_len,
+                             sm_scale, split_chunk, workspace, dev_error=None, stream=None):
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_split(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), int(max_seq_len), B, hq, k_cache.shape[1], d,
+        k_cache.shape[0], float(sm_scale), int(split_chunk), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_decode_split", st)
+
+
+def k16v8_merge_states(partial_o, partial_lse, seq_lens, split_chunk, out, lse=None,
+                       stream=None):
+    B, hq, C, d = partial_o.shape
+    st = load_library().k16v8_merge_states(
+        _ptr(partial_o), _ptr(partial_lse), B, hq, C, d, _ptr(seq_lens), int(split_chunk),
+        _ptr(out), _ptr(lse), _stream(stream))
+    _check("k16v8_merge_states", st)
+
+
+def k16v8_paged_decode_attention(q, k_cache, v_cache, v_scale, block_table, seq_lens,
+                                 max_seq_len, sm_scale, split_chunk, workspace, out, lse=None,
+                                 dev_error=None, stream=None):
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), int(max_seq_len), B, hq, k_cache.shape[1], d,
+        k_cache.shape[0], float(sm_scale), int(split_chunk), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _ptr(dev_error),
+        _stream(stream))
+    _check("k16v8_paged_decode_attention", st)
+
+
+def k16v8_read_device_error(dev_error, stream=None) -> int:
+    """Synchronise the stream and return the device error word."""
+    v = _i32()
+    st = load_library().k16v8_read_device_error(_ptr(dev_error), _stream(stream),
+                                                ctypes.byref(v))
+    if st not in (K16V8_OK, K16V8_ERR_DEVICE_BOUNDS):
+        _check("k16v8_read_device_error", st)
+    return int(v.value)

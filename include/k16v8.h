@@ -1,0 +1,205 @@
+/*
+ * k16v8.h -- C ABI of libk16v8.so: paged grouped-query attention over an
+ * asymmetric KV cache that keeps keys in FP16 and values in E4M3 FP8 with one
+ * FP32 scale per (layer, KV head) -- the "K16/V8" route of
+ * "Phi-4: quality transfer and interrupted throughput studies" (knlp.io).
+ *
+ * What the page fixes (intro section): the candidate stores FP16 keys and
+ * E4M3 FP8 values with the model's own scales, in a per-layer token-slot pool
+ * of a 32 GiB budget; the geometry is 40 layers, 40 query heads, 10 KV heads,
+ * head dimension 128.  Section "Matched diagnostic profiles" names the work
+ * this library implements: the attention kernels, the merge kernels, and the
+ * value gather that writes the compressed cache.
+ *
+ * Conventions shared by every call
+ *  - Pointers named as device pointers must point to device memory of the
+ *    current device; the caller owns all memory.  The library allocates
+ *    nothing and keeps no state between calls.
+ *  - Every launching call is asynchronous on `stream` (a cudaStream_t passed
+ *    as void*; NULL is the legacy default stream).  Only
+ *    k16v8_read_device_error synchronises.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    non-OK status means nothing was launched.
+ *  - Cache layout (pages of K16V8_PAGE_SIZE tokens), element (page, kv head,
+ *    offset, d) at ((page*num_kv_heads + head)*16 + offset)*head_dim + d:
+ *      k_cache  fp16  [num_pages][num_kv_heads][16][head_dim]
+ *      v_cache  E4M3  [num_pages][num_kv_heads][16][head_dim]  (one byte)
+ *      v_scale  fp32  [num_kv_heads]   value = v_scale[h] * e4m3(code)
+ *  - A slot is page*16 + offset.  block_table[b][i] holds the page of
+ *    positions 16i..16i+15 of sequence b.
+ *  - Supported shapes: head_dim == 128; attention calls need
+ *    num_qo_heads == 4*num_kv_heads (query head h reads KV head h/4).  Other
+ *    shapes return K16V8_ERR_UNSUPPORTED_SHAPE.
+ *  - Out-of-range slots, page ids or sequence lengths met on the device are
+ *    never dereferenced: the kernel skips or masks them and ORs a
+ *    K16V8_DEVERR_* bit into the caller's int32 error word (if non-NULL),
+ *    which k16v8_read_device_error returns.
+ */
+#ifndef K16V8_H
+#define K16V8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K16V8_PAGE_SIZE 16
+#define K16V8_HEAD_DIM 128
+#define K16V8_GQA_GROUP 4
+#define K16V8_MAX_SPLIT_CHUNK 8192
+
+typedef enum {
+    K16V8_OK = 0,
+    K16V8_ERR_INVALID_ARG = 1,        /* null pointer, negative size, misalignment */
+    K16V8_ERR_UNSUPPORTED_SHAPE = 2,  /* head_dim / GQA group not supported */
+    K16V8_ERR_WORKSPACE_TOO_SMALL = 3,
+    K16V8_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
+    K16V8_ERR_DEVICE_BOUNDS = 5       /* returned by k16v8_read_device_error */
+} k16v8_status;
+
+typedef enum { K16V8_F16 = 0, K16V8_F32 = 1 } k16v8_dtype;
+
+/* Bits of the device error word. */
+#define K16V8_DEVERR_SLOT 0x1    /* kv_append: slot >= num_pages*16 */
+#define K16V8_DEVERR_PAGE 0x2    /* block_table entry outside [0, num_pages) */
+#define K16V8_DEVERR_SEQLEN 0x4  /* seq_len < 0, > max_seq_len, or > 16*max_pages_per_seq */
+#define K16V8_DEVERR_TIMEOUT 0x8 /* a bounded wait on an async copy gave up */
+
+/*
+ * kv_append -- "the candidate also gathers values and writes the compressed
+ * cache" ("Matched diagnostic profiles"); storage format from the intro.
+ *
+ * For every token t with slot s = slot_mapping[t] >= 0 and every KV head h:
+ *   k_cache[s/16][h][s%16][:] = k[t][h][:]                      (fp16 copy)
+ *   v_cache[s/16][h][s%16][:] = E4M3_rn_satfinite(fl32(v[t][h][:]) / v_scale[h])
+ * The division is IEEE fp32 round-to-nearest; the E4M3 rounding is
+ * round-to-nearest-even with finite overflow and +-inf saturating to +-448
+ * (NaN stays NaN).  Negative slots are skipped (padding).  Slots at or above
+ * num_pages*16 are skipped and flag K16V8_DEVERR_SLOT.  Duplicate slots in
+ * one call leave an unspecified one of the writers.
+ *
+ *   k              device, fp16 [num_tokens][num_kv_heads][head_dim], token
+ *                  stride k_token_stride elements (0 = num_kv_heads*head_dim)
+ *   v              device, fp16 or fp32 (v_dtype) likewise, v_token_stride
+ *   slot_mapping   device, int64 [num_tokens]
+ *   v_scale        device, fp32 [num_kv_heads]
+ *   k_cache/v_cache device, the layer's pool (written in place)
+ *   dev_error      device int32 word or NULL
+ * k, v, caches: 16-byte aligned; token strides multiples of 8 elements.
+ */
+int32_t k16v8_kv_append(const void *k, int64_t k_token_stride, const void *v,
+                        int32_t v_dtype, int64_t v_token_stride,
+                        const int64_t *slot_mapping, int32_t num_tokens,
+                        const float *v_scale, void *k_cache, uint8_t *v_cache,
+                        int32_t num_pages, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t *dev_error, void *stream);
+
+/*
+ * Workspace for split-KV decode: partial outputs fp32
+ * [batch][num_qo_heads][max_chunks][head_dim] followed by partial LSEs fp32
+ * [batch][num_qo_heads][max_chunks], max_chunks = ceil(max_seq_len /
+ * split_chunk) (at least 1), each region 256-byte aligned.  Returns 0 for
+ * invalid arguments.
+ */
+size_t k16v8_decode_workspace_size(int32_t batch, int32_t num_qo_heads,
+                                   int32_t head_dim, int32_t max_seq_len,
+                                   int32_t split_chunk);
+
+/* Byte offsets of the two workspace regions and max_chunks (host only). */
+int32_t k16v8_decode_workspace_layout(int32_t batch, int32_t num_qo_heads,
+                                      int32_t head_dim, int32_t max_seq_len,
+                                      int32_t split_chunk,
+                                      size_t *partial_o_offset,
+                                      size_t *partial_lse_offset,
+                                      int32_t *max_chunks);
+
+/*
+ * paged_decode_split -- the attention kernels of "Matched diagnostic
+ * profiles", split over the KV sequence.
+ *
+ * One decode query per sequence.  For sequence b, query head h (KV head
+ * g = h/4) and chunk c covering positions [c*split_chunk,
+ * min((c+1)*split_chunk, L_b)), with s_j = sm_scale * q[b][h].k_j and
+ * v_j = v_scale[g] * e4m3(v8_j):
+ *   m_c = max_j s_j,  l_c = sum_j exp(s_j - m_c),
+ *   partial_o[b][h][c][:] = sum_j exp(s_j - m_c) v_j / l_c
+ *   partial_lse[b][h][c]  = m_c + ln l_c           (natural log)
+ * Chunks at or beyond ceil(L_b / split_chunk) are not written.
+ *
+ *   q            device, fp16 [batch][num_qo_heads][head_dim], 16-B aligned
+ *   block_table  device, int32 [batch][max_pages_per_seq]
+ *   seq_lens     device, int32 [batch]; each <= max_seq_len (host hint that
+ *                sizes the grid without a device->host copy)
+ *   split_chunk  tokens per chunk: a multiple of 16 in [16, 8192]
+ *   workspace    device, >= k16v8_decode_workspace_size(...) bytes, 256-B
+ *                aligned; receives the partials
+ *   sm_scale     softmax scale (1/sqrt(head_dim) for plain attention)
+ */
+int32_t k16v8_paged_decode_split(const void *q, const void *k_cache,
+                                 const uint8_t *v_cache, const float *v_scale,
+                                 const int32_t *block_table,
+                                 int32_t max_pages_per_seq,
+                                 const int32_t *seq_lens, int32_t max_seq_len,
+                                 int32_t batch, int32_t num_qo_heads,
+                                 int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t num_pages, float sm_scale,
+                                 int32_t split_chunk, void *workspace,
+                                 size_t workspace_bytes, int32_t *dev_error,
+                                 void *stream);
+
+/*
+ * merge_states -- the merge kernels of "Matched diagnostic profiles": the
+ * log-sum-exp combination of split-KV partials.  For each (b, h), over the
+ * n_b = ceil(min(L_b, max_chunks*split_chunk) / split_chunk) live chunks:
+ *   lse = M + ln sum_c exp(lse_c - M)   (M = max_c lse_c)
+ *   out = sum_c exp(lse_c - lse) * o_c       -> fp16, lse -> fp32
+ * n_b == 0 (an empty sequence) gives out = 0, lse = -inf.
+ *
+ *   partial_o    device, fp32 [batch][num_qo_heads][max_chunks][head_dim]
+ *   partial_lse  device, fp32 [batch][num_qo_heads][max_chunks]
+ *   seq_lens     device, int32 [batch]
+ *   out          device, fp16 [batch][num_qo_heads][head_dim], 8-B aligned
+ *   lse          device, fp32 [batch][num_qo_heads] or NULL
+ */
+int32_t k16v8_merge_states(const float *partial_o, const float *partial_lse,
+                           int32_t batch, int32_t num_qo_heads,
+                           int32_t max_chunks, int32_t head_dim,
+                           const int32_t *seq_lens, int32_t split_chunk,
+                           void *out, float *lse, void *stream);
+
+/*
+ * paged_decode_attention -- k16v8_paged_decode_split followed by
+ * k16v8_merge_states on the same stream, writing fp16 out
+ * [batch][num_qo_heads][head_dim] and fp32 lse [batch][num_qo_heads] (lse may
+ * be NULL).  Arguments as for the two calls.
+ */
+int32_t k16v8_paged_decode_attention(const void *q, const void *k_cache,
+                                     const uint8_t *v_cache, const float *v_scale,
+                                     const int32_t *block_table,
+                                     int32_t max_pages_per_seq,
+                                     const int32_t *seq_lens, int32_t max_seq_len,
+                                     int32_t batch, int32_t num_qo_heads,
+                                     int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t num_pages, float sm_scale,
+                                     int32_t split_chunk, void *workspace,
+                                     size_t workspace_bytes, void *out, float *lse,
+                                     int32_t *dev_error, void *stream);
+
+/*
+ * Wait for `stream`, then copy the device error word to *host_value and
+ * return K16V8_OK when it is zero, K16V8_ERR_DEVICE_BOUNDS otherwise
+ * (K16V8_ERR_CUDA if the synchronisation or copy fails).
+ */
+int32_t k16v8_read_device_error(const int32_t *dev_error, void *stream,
+                                int32_t *host_value);
+
+/* Static, human-readable name of a status code. */
+const char *k16v8_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K16V8_H */

@@ -77,3 +77,32 @@ def check_close(out, ref, lse=None, lse_ref=None, atol=ATOL, rtol=RTOL, lse_tol=
         assert np.array_equal(np.isinf(lse), inf)
         d = np.abs(lse[~inf] - lse_ref[~inf])
         assert d.size == 0 or d.max() <= lse_tol, f"lse err {d.max():.3e}"
+
+
+# ---- GPU-side helpers (torch only moves memory; compute is in libk16v8) ----
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+
+
+def gpu_poisoned_caches(num_pages, hkv, d, page=16):
+    kc = torch.full((num_pages, hkv, page, d), int(np.int16(K_POISON.view(np.int16))),
+                    dtype=torch.int16, device=dev()).view(torch.float16)
+    vc = torch.full((num_pages, hkv, page, d), int(V_POISON), dtype=torch.uint8, device=dev())
+    return kc, vc
+
+
+def gpu_cache(w, K, err=None):
+    """Caches of a workload written by the library's kv_append."""
+    kc, vc = gpu_poisoned_caches(w.num_pages, w.num_kv_heads, w.head_dim, w.page_size)
+    K.k16v8_kv_append(to_dev(w.k_tok), to_dev(w.v_tok), to_dev(w.slot_mapping),
+                      to_dev(w.v_scale), kc, vc, err)
+    return kc, vc
+
+
+def host_bits(kc, vc):
+    return (kc.view(torch.int16).cpu().numpy().view(np.uint16), vc.cpu().numpy())
