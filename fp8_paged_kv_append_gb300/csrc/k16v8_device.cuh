@@ -133,6 +133,18 @@ static inline int32_t k16v8_launch_status() {
   return cudaGetLastError() == cudaSuccess ? K16V8_OK : K16V8_ERR_CUDA;
 }
 
+// SM count of the current device, cached per device (host only).
+static inline int k16v8_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cached[dev] = sms;
+  return sms;
+}
+
 static inline bool k16v8_aligned(const void *p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

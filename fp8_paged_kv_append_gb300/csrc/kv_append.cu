@@ -102,10 +102,8 @@ extern "C" int32_t k16v8_kv_append(const void *k, int64_t k_token_stride, const 
       !k16v8_aligned(v_scale, 4))
     return K16V8_ERR_INVALID_ARG;
 
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return K16V8_ERR_CUDA;
+  const int sms = k16v8_sm_count();
+  if (sms <= 0) return K16V8_ERR_CUDA;
   const int64_t units = static_cast<int64_t>(num_tokens) * num_kv_heads * (kHeadDim / 8);
   const int threads = 256;
   int64_t blocks = (units + threads - 1) / threads;
