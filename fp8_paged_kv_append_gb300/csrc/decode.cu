@@ -31,7 +31,8 @@
 namespace k16v8 {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 4;
+constexpr int kStages = 2;
+constexpr int kMinBlocks = 4;
 constexpr int kKPageBytes = kPage * kHeadDim * 2;  // 4096
 constexpr int kVPageBytes = kPage * kHeadDim;      // 2048
 constexpr unsigned kFull = 0xffffffffu;
@@ -39,8 +40,8 @@ constexpr unsigned kFull = 0xffffffffu;
 struct __align__(128) WarpRing {
   uint8_t k[kStages][kKPageBytes];
   uint8_t v[kStages][kVPageBytes];
-  float p[kPage * kGroup];  // p[token][head] of the page being consumed
-  float alpha[kGroup];      // rescale factor of the running state
+  uint16_t p[kPage * kGroup];  // fp16 p[token][head] of the page being consumed
+  float alpha[kGroup];         // rescale factor of the running state
   uint64_t bar[kStages];
 };
 
@@ -49,18 +50,41 @@ static size_t decode_smem_bytes(int split_chunk) {
   return kWarps * sizeof(WarpRing) + ((ids + 15) / 16) * 16;
 }
 
-__device__ __forceinline__ void dot8(const uint4 &raw, const float (&qf)[kGroup][16], int base,
-                                     float (&acc)[kGroup]) {
-  const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(h2[i]);
-#pragma unroll
-    for (int h = 0; h < kGroup; ++h) {
-      acc[h] = fmaf(qf[h][base + 2 * i], f.x, acc[h]);
-      acc[h] = fmaf(qf[h][base + 2 * i + 1], f.y, acc[h]);
-    }
-  }
+// acc += a.lo * b.lo + a.hi * b.hi with fp16 operands, fp32 accumulation
+// (each product is exact in fp32; one rounding per FMA).
+__device__ __forceinline__ float fma_h2(uint32_t a, uint32_t b, float acc) {
+  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+      "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(a), "r"(b));
+  return acc;
+}
+
+// acc[0..3] += p(f16 scalar, from a packed pair) * v(4 x f16 in two pairs)
+__device__ __forceinline__ void fma_pv(uint32_t p2, bool hi, uint32_t v01, uint32_t v23,
+                                       float (&o)[4]) {
+  if (hi)
+    asm("{\n\t.reg .f16 pl, ph, x0, x1, x2, x3;\n\t"
+        "mov.b32 {pl, ph}, %4;\n\tmov.b32 {x0, x1}, %5;\n\tmov.b32 {x2, x3}, %6;\n\t"
+        "fma.rn.f32.f16 %0, ph, x0, %0;\n\tfma.rn.f32.f16 %1, ph, x1, %1;\n\t"
+        "fma.rn.f32.f16 %2, ph, x2, %2;\n\tfma.rn.f32.f16 %3, ph, x3, %3;\n\t}"
+        : "+f"(o[0]), "+f"(o[1]), "+f"(o[2]), "+f"(o[3])
+        : "r"(p2), "r"(v01), "r"(v23));
+  else
+    asm("{\n\t.reg .f16 pl, ph, x0, x1, x2, x3;\n\t"
+        "mov.b32 {pl, ph}, %4;\n\tmov.b32 {x0, x1}, %5;\n\tmov.b32 {x2, x3}, %6;\n\t"
+        "fma.rn.f32.f16 %0, pl, x0, %0;\n\tfma.rn.f32.f16 %1, pl, x1, %1;\n\t"
+        "fma.rn.f32.f16 %2, pl, x2, %2;\n\tfma.rn.f32.f16 %3, pl, x3, %3;\n\t}"
+        : "+f"(o[0]), "+f"(o[1]), "+f"(o[2]), "+f"(o[3])
+        : "r"(p2), "r"(v01), "r"(v23));
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_h2bits(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
 }
 
 // Sum acc[0..3] over the 8 lanes of a token group; lane j of the group ends
@@ -81,7 +105,7 @@ __device__ __forceinline__ float reduce_scatter8(const float (&acc)[kGroup], int
   return kp;
 }
 
-__global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(
+__global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
     const __half *__restrict__ q, const __half *__restrict__ k_cache,
     const uint8_t *__restrict__ v_cache, const float *__restrict__ v_scale,
     const int32_t *__restrict__ block_table, int32_t maxp, const int32_t *__restrict__ seq_lens,
@@ -141,38 +165,34 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(
   if (lane == 0)
     for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
 
-  // Query of the group's 4 heads, pre-multiplied by sm_scale*log2(e).
-  // Lane j of a token group owns dims [8j, 8j+8) and [64+8j, 64+8j+8).
+  // Query of the group's 4 heads as packed fp16 pairs.  Lane j of a token
+  // group owns dims [8j, 8j+8) and [64+8j, 64+8j+8): qh[h][0..3], qh[h][4..7].
   const int j = lane & 7;
-  float qf[kGroup][16];
+  uint32_t qh[kGroup][8];
   {
-    const float qs = sm_scale * kLog2e;
     const __half *qb = q + (static_cast<int64_t>(b) * hq + g * kGroup) * kHeadDim;
 #pragma unroll
     for (int h = 0; h < kGroup; ++h) {
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qb + h * kHeadDim + part * 64 + j * 8));
-        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(h2[i]);
-          qf[h][part * 8 + 2 * i] = f.x * qs;
-          qf[h][part * 8 + 2 * i + 1] = f.y * qs;
-        }
+        const uint4 raw =
+            __ldg(reinterpret_cast<const uint4 *>(qb + h * kHeadDim + part * 64 + j * 8));
+        qh[h][part * 4 + 0] = raw.x;
+        qh[h][part * 4 + 1] = raw.y;
+        qh[h][part * 4 + 2] = raw.z;
+        qh[h][part * 4 + 3] = raw.w;
       }
     }
   }
+  const float qs = sm_scale * kLog2e;  // scores in the log2 domain
 
-  const int hsel = j >> 1;            // head whose score this lane holds
-  const int d0 = (lane & 15) * 8;     // P.V: this lane's 8 dims
-  const int tpar = lane >> 4;         // P.V: token parity handled
+  const int hsel = j >> 1;  // head whose score this lane holds
   float m_run = -INFINITY, l_run = 0.f;
-  float o[kGroup][8];
+  float o[kGroup][4];  // P.V: this lane's dims [4*lane, 4*lane+4)
 #pragma unroll
   for (int h = 0; h < kGroup; ++h)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+    for (int e = 0; e < 4; ++e) o[h][e] = 0.f;
 
   int k = 0;
   bool ok = true;
@@ -191,10 +211,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(
         const int t = it * 4 + (lane >> 3);
         const uint4 a = *reinterpret_cast<const uint4 *>(kp + t * 256 + j * 16);
         const uint4 bq = *reinterpret_cast<const uint4 *>(kp + t * 256 + 128 + j * 16);
-        float acc[kGroup] = {0.f, 0.f, 0.f, 0.f};
-        dot8(a, qf, 0, acc);
-        dot8(bq, qf, 8, acc);
-        const float v = reduce_scatter8(acc, j);
+        float acc[kGroup], acc2[kGroup];
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          acc[h] = fma_h2(qh[h][0], a.x, 0.f);
+          acc2[h] = fma_h2(qh[h][4], bq.x, 0.f);
+          acc[h] = fma_h2(qh[h][1], a.y, acc[h]);
+          acc2[h] = fma_h2(qh[h][5], bq.y, acc2[h]);
+          acc[h] = fma_h2(qh[h][2], a.z, acc[h]);
+          acc2[h] = fma_h2(qh[h][6], bq.z, acc2[h]);
+          acc[h] = fma_h2(qh[h][3], a.w, acc[h]);
+          acc2[h] = fma_h2(qh[h][7], bq.w, acc2[h]);
+          acc[h] += acc2[h];
+        }
+        const float v = reduce_scatter8(acc, j) * qs;
         sc[it] = t < valid ? v : -INFINITY;
       }
       // ---- online softmax (log2 domain) ----
@@ -210,41 +240,32 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(
       m_run = m_new;
       if ((lane & 1) == 0) {
 #pragma unroll
-        for (int it = 0; it < 4; ++it) ring.p[(it * 4 + (lane >> 3)) * kGroup + hsel] = p[it];
+        for (int it = 0; it < 4; ++it)
+          ring.p[(it * 4 + (lane >> 3)) * kGroup + hsel] = __half_as_ushort(__float2half_rn(p[it]));
         if (lane < 8) ring.alpha[hsel] = alpha;
       }
       __syncwarp();
-      // ---- P.V over this page ----
+      // ---- P.V over this page: lane owns 4 dims of every token ----
       const float4 al = *reinterpret_cast<const float4 *>(ring.alpha);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
+      for (int e = 0; e < 4; ++e) {
         o[0][e] *= al.x;
         o[1][e] *= al.y;
         o[2][e] *= al.z;
         o[3][e] *= al.w;
       }
-      const uint8_t *vp = ring.v[s];
+      const uint8_t *vp = ring.v[s] + lane * 4;
 #pragma unroll
-      for (int tt = 0; tt < kPage / 2; ++tt) {
-        const int t = 2 * tt + tpar;
+      for (int t = 0; t < kPage; ++t) {
         if (t < valid) {
-          const uint2 raw = *reinterpret_cast<const uint2 *>(vp + t * kHeadDim + d0);
-          const float4 pp = *reinterpret_cast<const float4 *>(ring.p + t * kGroup);
-          float vf[8];
-          const uint16_t *pr = reinterpret_cast<const uint16_t *>(&raw);
-#pragma unroll
-          for (int i2 = 0; i2 < 4; ++i2) {
-            const float2 f = __half22float2(e4m3x2_to_half2(pr[i2]));
-            vf[2 * i2] = f.x;
-            vf[2 * i2 + 1] = f.y;
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            o[0][e] = fmaf(pp.x, vf[e], o[0][e]);
-            o[1][e] = fmaf(pp.y, vf[e], o[1][e]);
-            o[2][e] = fmaf(pp.z, vf[e], o[2][e]);
-            o[3][e] = fmaf(pp.w, vf[e], o[3][e]);
-          }
+          const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp + t * kHeadDim);
+          const uint2 pp = *reinterpret_cast<const uint2 *>(ring.p + t * kGroup);
+          const uint32_t v01 = e4m3x2_to_h2bits(static_cast<uint16_t>(raw & 0xffffu));
+          const uint32_t v23 = e4m3x2_to_h2bits(static_cast<uint16_t>(raw >> 16));
+          fma_pv(pp.x, false, v01, v23, o[0]);
+          fma_pv(pp.x, true, v01, v23, o[1]);
+          fma_pv(pp.y, false, v01, v23, o[2]);
+          fma_pv(pp.y, true, v01, v23, o[3]);
         }
       }
     }
@@ -265,11 +286,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(
     __syncwarp();
   }
 
-  // ---- combine the token-parity halves and the lanes of each head ----
-#pragma unroll
-  for (int h = 0; h < kGroup; ++h)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(kFull, o[h][e], 16);
+  // ---- sum each head's l over its lanes (lanes j, j^1 hold copies) ----
   l_run += __shfl_xor_sync(kFull, l_run, 8);
   l_run += __shfl_xor_sync(kFull, l_run, 16);
 
@@ -282,14 +299,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(
     wm[warp * kGroup + hsel] = m_run;
     wl[warp * kGroup + hsel] = l_run;
   }
-  if (lane < 16) {
 #pragma unroll
-    for (int h = 0; h < kGroup; ++h) {
-      float *dst = wo + (warp * kGroup + h) * kHeadDim + d0;
-      *reinterpret_cast<float4 *>(dst) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-      *reinterpret_cast<float4 *>(dst + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
-    }
-  }
+  for (int h = 0; h < kGroup; ++h)
+    *reinterpret_cast<float4 *>(wo + (warp * kGroup + h) * kHeadDim + lane * 4) =
+        make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
   __syncthreads();
   {
     const int h = threadIdx.x >> 5;
@@ -316,15 +329,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(
     if (Ls > 0.f) {
       const float inv = __ldg(v_scale + g) / Ls;
       res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      lse = (M + log2f(Ls)) * kLn2;
+      lse = (M + lg2(Ls)) * kLn2;
     }
     *reinterpret_cast<float4 *>(part_o + row * kHeadDim + d4) = res;
     if ((threadIdx.x & 31) == 0) part_lse[row] = lse;
   }
 }
 
-// One warp per (sequence, query head); lane owns 4 dims.
-__global__ void __launch_bounds__(128) merge_states_kernel(
+// One warp per (sequence, query head); lane owns 4 dims.  The live chunks'
+// LSEs are loaded lane-parallel; partial rows are read 4 at a time so their
+// loads are in flight together.
+__global__ void __launch_bounds__(128, 8) merge_states_kernel(
     const float *__restrict__ part_o, const float *__restrict__ part_lse, int32_t rows,
     int32_t hq, int32_t max_chunks, const int32_t *__restrict__ seq_lens, int32_t chunk,
     __half *__restrict__ out, float *__restrict__ lse_out) {
@@ -338,27 +353,46 @@ __global__ void __launch_bounds__(128) merge_states_kernel(
   const float *pl = part_lse + static_cast<int64_t>(wid) * max_chunks;
   const float *po = part_o + static_cast<int64_t>(wid) * max_chunks * kHeadDim + lane * 4;
   float M = -INFINITY;
-  for (int c = lane; c < nc; c += 32) M = fmaxf(M, pl[c]);
+  for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldg(pl + c));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
   float S = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int c = 0; c < nc; ++c) {
-      const float w = ex2((pl[c] - M) * kLog2e);
-      const float4 oc = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(c) * kHeadDim);
-      S += w;
-      acc.x = fmaf(w, oc.x, acc.x);
-      acc.y = fmaf(w, oc.y, acc.y);
-      acc.z = fmaf(w, oc.z, acc.z);
-      acc.w = fmaf(w, oc.w, acc.w);
+    int c = 0;
+    for (; c + 4 <= nc; c += 4) {
+      float4 oc[4];
+      float w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        oc[u] = __ldg(reinterpret_cast<const float4 *>(po + static_cast<int64_t>(c + u) * kHeadDim));
+        w[u] = __ldg(pl + c + u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wu = ex2((w[u] - M) * kLog2e);
+        S += wu;
+        acc.x = fmaf(wu, oc[u].x, acc.x);
+        acc.y = fmaf(wu, oc[u].y, acc.y);
+        acc.z = fmaf(wu, oc[u].z, acc.z);
+        acc.w = fmaf(wu, oc[u].w, acc.w);
+      }
+    }
+    for (; c < nc; ++c) {
+      const float4 oc = __ldg(reinterpret_cast<const float4 *>(po + static_cast<int64_t>(c) * kHeadDim));
+      const float wu = ex2((__ldg(pl + c) - M) * kLog2e);
+      S += wu;
+      acc.x = fmaf(wu, oc.x, acc.x);
+      acc.y = fmaf(wu, oc.y, acc.y);
+      acc.z = fmaf(wu, oc.z, acc.z);
+      acc.w = fmaf(wu, oc.w, acc.w);
     }
   }
   float lse = -INFINITY;
   if (S > 0.f) {
-    const float inv = 1.f / S;
+    const float inv = rcp(S);
     acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    lse = M + logf(S);
+    lse = M + lg2(S) * kLn2;
   }
   uint2 st;
   st.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.x))) |

@@ -105,6 +105,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Two fp32 -> two E4M3FN bytes, round-to-nearest-even, saturating finite
 // values (hardware cvt).  Result: lo byte <- x0, hi byte <- x1.
 __device__ __forceinline__ uint16_t e4m3x2_from_f32(float x0, float x1) {
