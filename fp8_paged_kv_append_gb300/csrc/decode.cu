@@ -40,7 +40,7 @@ constexpr unsigned kFull = 0xffffffffu;
 struct __align__(128) WarpRing {
   uint8_t k[kStages][kKPageBytes];
   uint8_t v[kStages][kVPageBytes];
-  uint16_t p[kPage * kGroup];  // fp16 p[token][head] of the page being consumed
+  uint32_t p[kPage * kGroup];  // p[token][head] as a duplicated fp16 pair (p, p)
   float alpha[kGroup];         // rescale factor of the running state
   uint64_t bar[kStages];
 };
@@ -60,25 +60,6 @@ __device__ __forceinline__ float fma_h2(uint32_t a, uint32_t b, float acc) {
       : "+f"(acc)
       : "r"(a), "r"(b));
   return acc;
-}
-
-// acc[0..3] += p(f16 scalar, from a packed pair) * v(4 x f16 in two pairs)
-__device__ __forceinline__ void fma_pv(uint32_t p2, bool hi, uint32_t v01, uint32_t v23,
-                                       float (&o)[4]) {
-  if (hi)
-    asm("{\n\t.reg .f16 pl, ph, x0, x1, x2, x3;\n\t"
-        "mov.b32 {pl, ph}, %4;\n\tmov.b32 {x0, x1}, %5;\n\tmov.b32 {x2, x3}, %6;\n\t"
-        "fma.rn.f32.f16 %0, ph, x0, %0;\n\tfma.rn.f32.f16 %1, ph, x1, %1;\n\t"
-        "fma.rn.f32.f16 %2, ph, x2, %2;\n\tfma.rn.f32.f16 %3, ph, x3, %3;\n\t}"
-        : "+f"(o[0]), "+f"(o[1]), "+f"(o[2]), "+f"(o[3])
-        : "r"(p2), "r"(v01), "r"(v23));
-  else
-    asm("{\n\t.reg .f16 pl, ph, x0, x1, x2, x3;\n\t"
-        "mov.b32 {pl, ph}, %4;\n\tmov.b32 {x0, x1}, %5;\n\tmov.b32 {x2, x3}, %6;\n\t"
-        "fma.rn.f32.f16 %0, pl, x0, %0;\n\tfma.rn.f32.f16 %1, pl, x1, %1;\n\t"
-        "fma.rn.f32.f16 %2, pl, x2, %2;\n\tfma.rn.f32.f16 %3, pl, x3, %3;\n\t}"
-        : "+f"(o[0]), "+f"(o[1]), "+f"(o[2]), "+f"(o[3])
-        : "r"(p2), "r"(v01), "r"(v23));
 }
 
 __device__ __forceinline__ uint32_t e4m3x2_to_h2bits(uint16_t v) {
@@ -188,11 +169,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
 
   const int hsel = j >> 1;  // head whose score this lane holds
   float m_run = -INFINITY, l_run = 0.f;
-  float o[kGroup][4];  // P.V: this lane's dims [4*lane, 4*lane+4)
+  // P.V state: this lane's dims [4*lane, 4*lane+4) of the 4 heads, fp32
+  // across pages; within a page the products accumulate as fp16 pairs
+  // (p <= 1 and |v| <= 448, so a 16-token page sum stays below 7168).
+  float2 o[kGroup][2];
 #pragma unroll
-  for (int h = 0; h < kGroup; ++h)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[h][e] = 0.f;
+  for (int h = 0; h < kGroup; ++h) o[h][0] = o[h][1] = make_float2(0.f, 0.f);
 
   int k = 0;
   bool ok = true;
@@ -240,33 +222,45 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
       m_run = m_new;
       if ((lane & 1) == 0) {
 #pragma unroll
-        for (int it = 0; it < 4; ++it)
-          ring.p[(it * 4 + (lane >> 3)) * kGroup + hsel] = __half_as_ushort(__float2half_rn(p[it]));
+        for (int it = 0; it < 4; ++it) {
+          const uint32_t ph = __half_as_ushort(__float2half_rn(p[it]));
+          ring.p[(it * 4 + (lane >> 3)) * kGroup + hsel] = ph | (ph << 16);
+        }
         if (lane < 8) ring.alpha[hsel] = alpha;
       }
       __syncwarp();
       // ---- P.V over this page: lane owns 4 dims of every token ----
-      const float4 al = *reinterpret_cast<const float4 *>(ring.alpha);
+      __half2 acc[kGroup][2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        o[0][e] *= al.x;
-        o[1][e] *= al.y;
-        o[2][e] *= al.z;
-        o[3][e] *= al.w;
-      }
+      for (int h = 0; h < kGroup; ++h) acc[h][0] = acc[h][1] = __float2half2_rn(0.f);
       const uint8_t *vp = ring.v[s] + lane * 4;
+      auto pv_token = [&](int t) {
+        const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp + t * kHeadDim);
+        const uint4 pp = *reinterpret_cast<const uint4 *>(ring.p + t * kGroup);
+        const __half2 v01 = e4m3x2_to_half2(static_cast<uint16_t>(raw & 0xffffu));
+        const __half2 v23 = e4m3x2_to_half2(static_cast<uint16_t>(raw >> 16));
+        const uint32_t pw[kGroup] = {pp.x, pp.y, pp.z, pp.w};
 #pragma unroll
-      for (int t = 0; t < kPage; ++t) {
-        if (t < valid) {
-          const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp + t * kHeadDim);
-          const uint2 pp = *reinterpret_cast<const uint2 *>(ring.p + t * kGroup);
-          const uint32_t v01 = e4m3x2_to_h2bits(static_cast<uint16_t>(raw & 0xffffu));
-          const uint32_t v23 = e4m3x2_to_h2bits(static_cast<uint16_t>(raw >> 16));
-          fma_pv(pp.x, false, v01, v23, o[0]);
-          fma_pv(pp.x, true, v01, v23, o[1]);
-          fma_pv(pp.y, false, v01, v23, o[2]);
-          fma_pv(pp.y, true, v01, v23, o[3]);
+        for (int h = 0; h < kGroup; ++h) {
+          const __half2 ph = *reinterpret_cast<const __half2 *>(&pw[h]);
+          acc[h][0] = __hfma2(ph, v01, acc[h][0]);
+          acc[h][1] = __hfma2(ph, v23, acc[h][1]);
         }
+      };
+      if (valid == kPage) {
+#pragma unroll
+        for (int t = 0; t < kPage; ++t) pv_token(t);
+      } else {
+        for (int t = 0; t < valid; ++t) pv_token(t);
+      }
+      // fold the page into the fp32 state: o = o * alpha + page sum
+      const float4 al = *reinterpret_cast<const float4 *>(ring.alpha);
+      const float alv[kGroup] = {al.x, al.y, al.z, al.w};
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+        const float2 a2 = make_float2(alv[h], alv[h]);
+        o[h][0] = __ffma2_rn(o[h][0], a2, __half22float2(acc[h][0]));
+        o[h][1] = __ffma2_rn(o[h][1], a2, __half22float2(acc[h][1]));
       }
     }
     __syncwarp();
@@ -302,7 +296,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
 #pragma unroll
   for (int h = 0; h < kGroup; ++h)
     *reinterpret_cast<float4 *>(wo + (warp * kGroup + h) * kHeadDim + lane * 4) =
-        make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
   __syncthreads();
   {
     const int h = threadIdx.x >> 5;
