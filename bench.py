@@ -422,6 +422,8 @@ def main():
                     help="skip the secondary 8K/b16 line inside the JSON")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--split-chunk", type=int, default=0,
+                    help="tokens per split-KV chunk of the main workload (0: its default)")
     args = ap.parse_args()
     rank, world, local_rank = dist_env()
 
@@ -440,6 +442,8 @@ def main():
 
     # Replicas only: every rank runs the same seeded workload on its own GPU.
     w, label, chunk = make_workload(args.workload)
+    if args.split_chunk:
+        chunk = args.split_chunk
     bench = DecodeBench(w, device, split_chunk=chunk)
     clocks = ClockSampler(local_rank).start()
     ms, seg = bench.run(args.steps, max(args.warmup, 3))

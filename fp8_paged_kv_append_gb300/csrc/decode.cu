@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
 
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
 
   int L = __ldg(seq_lens + b);
   const int cap = min(maxp * kPage, max_chunks * chunk);
@@ -280,6 +281,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
     __syncwarp();
   }
 
+  pdl_launch_dependents();
+
   // ---- sum each head's l over its lanes (lanes j, j^1 hold copies) ----
   l_run += __shfl_xor_sync(kFull, l_run, 8);
   l_run += __shfl_xor_sync(kFull, l_run, 16);
@@ -339,6 +342,8 @@ __global__ void __launch_bounds__(128, 8) merge_states_kernel(
     __half *__restrict__ out, float *__restrict__ lse_out) {
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_launch_dependents();
   if (wid >= rows) return;
   const int b = wid / hq;
   int L = __ldg(seq_lens + b);
@@ -495,11 +500,11 @@ extern "C" int32_t k16v8_paged_decode_split(
   float *po = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_off);
   float *pl = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.lse_off);
   const dim3 grid(w.chunks, num_kv_heads, batch);
-  decode_split_kernel<<<grid, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __half *>(q), static_cast<const __half *>(k_cache), v_cache, v_scale,
-      block_table, max_pages_per_seq, seq_lens, num_qo_heads, num_kv_heads, num_pages, sm_scale,
-      split_chunk, w.chunks, po, pl, dev_error);
-  return k16v8_launch_status();
+  return k16v8_launch_pdl(decode_split_kernel, grid, dim3(kWarps * 32), smem,
+                          static_cast<cudaStream_t>(stream), static_cast<const __half *>(q),
+                          static_cast<const __half *>(k_cache), v_cache, v_scale, block_table,
+                          max_pages_per_seq, seq_lens, num_qo_heads, num_kv_heads, num_pages,
+                          sm_scale, split_chunk, w.chunks, po, pl, dev_error);
 }
 
 extern "C" int32_t k16v8_merge_states(const float *partial_o, const float *partial_lse,
@@ -518,10 +523,10 @@ extern "C" int32_t k16v8_merge_states(const float *partial_o, const float *parti
   const int64_t rows = static_cast<int64_t>(batch) * num_qo_heads;
   if (rows > (1LL << 31) - 4) return K16V8_ERR_INVALID_ARG;
   const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
-  merge_states_kernel<<<blocks, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-      partial_o, partial_lse, static_cast<int32_t>(rows), num_qo_heads, max_chunks, seq_lens,
-      split_chunk, static_cast<__half *>(out), lse);
-  return k16v8_launch_status();
+  return k16v8_launch_pdl(merge_states_kernel, dim3(blocks), dim3(128), 0,
+                          static_cast<cudaStream_t>(stream), partial_o, partial_lse,
+                          static_cast<int32_t>(rows), num_qo_heads, max_chunks, seq_lens,
+                          split_chunk, static_cast<__half *>(out), lse);
 }
 
 extern "C" int32_t k16v8_paged_decode_attention(

@@ -134,6 +134,14 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint16_t v) {
   return h;
 }
 
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible (a no-op without the launch
+// attribute), and allow the next grid to begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_error(int32_t *dev_error, int32_t bit) {
   if (dev_error) atomicOr(dev_error, bit);
 }
@@ -155,6 +163,27 @@ static inline int k16v8_sm_count() {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   if (dev < 64) cached[dev] = sms;
   return sms;
+}
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous grid of the stream drains; every k16v8 kernel executes
+// griddepcontrol.wait before it reads anything, so ordering is unchanged.
+template <typename... KArgs, typename... Args>
+static inline int32_t k16v8_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                       size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess
+             ? K16V8_OK
+             : K16V8_ERR_CUDA;
 }
 
 static inline bool k16v8_aligned(const void *p, size_t a) {

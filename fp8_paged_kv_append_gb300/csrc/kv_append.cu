@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const float *__restrict__ v_scale, __half *__restrict__ k_cache,
     uint8_t *__restrict__ v_cache, int32_t num_pages, int32_t hkv, int32_t *dev_error) {
   constexpr int kVecPerRow = kHeadDim / 8;  // 16 threads per row
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t units = static_cast<int64_t>(num_tokens) * hkv * kVecPerRow;
   const int64_t n_slots = static_cast<int64_t>(num_pages) * kPage;
   for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
@@ -110,15 +112,14 @@ extern "C" int32_t k16v8_kv_append(const void *k, int64_t k_token_stride, const 
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 resident CTAs of 256 per SM
   if (blocks > cap) blocks = cap;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dim3 grid(static_cast<unsigned>(blocks)), block(threads);
   if (v_dtype == K16V8_F32)
-    kv_append_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-        static_cast<const __half *>(k), k_token_stride, v, v_token_stride, slot_mapping,
-        num_tokens, v_scale, static_cast<__half *>(k_cache), v_cache, num_pages, num_kv_heads,
-        dev_error);
-  else
-    kv_append_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-        static_cast<const __half *>(k), k_token_stride, v, v_token_stride, slot_mapping,
-        num_tokens, v_scale, static_cast<__half *>(k_cache), v_cache, num_pages, num_kv_heads,
-        dev_error);
-  return k16v8_launch_status();
+    return k16v8_launch_pdl(kv_append_kernel<true>, grid, block, 0, s,
+                            static_cast<const __half *>(k), k_token_stride, v, v_token_stride,
+                            slot_mapping, num_tokens, v_scale, static_cast<__half *>(k_cache),
+                            v_cache, num_pages, num_kv_heads, dev_error);
+  return k16v8_launch_pdl(kv_append_kernel<false>, grid, block, 0, s,
+                          static_cast<const __half *>(k), k_token_stride, v, v_token_stride,
+                          slot_mapping, num_tokens, v_scale, static_cast<__half *>(k_cache),
+                          v_cache, num_pages, num_kv_heads, dev_error);
 }
