@@ -32,22 +32,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-def make_event():
-    import torch
-    return torch.cuda.Event(enable_timing=True, external=True)
-
-
-def _external_events_supported():
-    try:
-        import torch
-        torch.cuda.Event(enable_timing=True, external=True)
-        return True
-    except TypeError:
-        return False
-
-
-EXTERNAL_EVENTS = _external_events_supported()
-
 METRIC = "K16/V8 paged decode attention: KV GB/s vs HBM peak; µs per layer-step"
 L2_BYTES = 129 * 10 ** 6
 
@@ -220,15 +204,15 @@ class DecodeBench:
         if ev:
             ev[3].record()
 
-    def capture(self, steps, with_events):
-        """One CUDA graph per step (kernel launches + timing-event nodes), so
-        the timed region replays pre-built launches without host overhead."""
+    def capture(self, steps, with_events=False):
+        """One CUDA graph per step, so the timed region replays pre-built
+        launches without host overhead."""
         torch = self.torch
         side = torch.cuda.Stream(self.dev)
         graphs, evs = [], []
         for i in range(steps):
             g = torch.cuda.CUDAGraph()
-            e = [make_event() for _ in range(4)] if with_events else None
+            e = None
             with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
                 self.step(i, e)
             graphs.append(g)
@@ -237,11 +221,15 @@ class DecodeBench:
         return graphs, evs
 
     def run(self, steps, warmup):
+        """Time `steps` replays of per-step graphs (no timing nodes inside, so
+        programmatic launch edges between the kernels stay intact), then the
+        average duration of each kernel from a graph of `steps` launches of
+        that kernel alone over the same state."""
         torch = self.torch
         for i in range(warmup):  # eager warm-up also configures kernel attributes
             self.step(i)
         torch.cuda.synchronize(self.dev)
-        graphs, evs = self.capture(steps, with_events=EXTERNAL_EVENTS)
+        graphs, _ = self.capture(steps, with_events=False)
         for i in range(warmup):
             graphs[i % steps].replay()
         torch.cuda.synchronize(self.dev)
@@ -256,18 +244,14 @@ class DecodeBench:
         torch.cuda.synchronize(self.dev)
         barrier()
         total_ms = t0.elapsed_time(t1)
-        if EXTERNAL_EVENTS:
-            seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]),
-                             e[2].elapsed_time(e[3])] for e in evs])
-        else:
-            seg = self.per_kernel_fallback(steps)
+        seg = self.per_kernel(steps)
         if self.K.k16v8_read_device_error(self.err) != 0:
             raise RuntimeError("device error flag raised during the benchmark")
         return total_ms / steps, seg
 
-    def per_kernel_fallback(self, steps):
-        """Per-kernel durations when timing events cannot be graph nodes:
-        one graph per kernel kind, `steps` launches each, timed as a block."""
+    def per_kernel(self, steps):
+        """Average launch duration per kernel: one graph per kernel kind with
+        `steps` launches (rotating over the pool replicas), timed as a block."""
         torch, K = self.torch, self.K
         outs = []
         kinds = [
@@ -293,7 +277,7 @@ class DecodeBench:
             t1.record()
             torch.cuda.synchronize(self.dev)
             outs.append(t0.elapsed_time(t1) / steps)
-        return np.array([outs] * steps)
+        return np.array([outs])
 
     def run_e2e(self, steps, warmup):
         """Same step through host buffers: pinned H2D of the step's inputs, the
