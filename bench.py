@@ -381,7 +381,7 @@ def run_cpu_baseline(w, chunk, budget_s=12.0):
 def make_workload(name):
     from fp8_paged_kv_append_gb300 import workloads
     if name == "1k":
-        return workloads.decode_1k_b32(), "decode 1K/batch 32", 512
+        return workloads.decode_1k_b32(), "decode 1K/batch 32", 384
     if name == "8k":
         return workloads.decode_8k_b16(), "decode 8K/batch 16", 512
     raise SystemExit(f"unknown workload {name}")
