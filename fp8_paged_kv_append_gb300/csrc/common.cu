@@ -21,6 +21,8 @@ extern "C" const char *k16v8_status_string(int32_t status) {
     case K16V8_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case K16V8_ERR_CUDA: return "CUDA error";
     case K16V8_ERR_DEVICE_BOUNDS: return "out-of-range index met on the device";
+    case K16V8_ERR_STATIC_SCRATCH_LIMIT:
+      return "problem needs more than the library's built-in scratch";
     default: return "unknown status";
   }
 }

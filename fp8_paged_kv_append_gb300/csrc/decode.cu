@@ -549,3 +549,52 @@ extern "C" int32_t k16v8_paged_decode_attention(
                             num_qo_heads, w.chunks, head_dim, seq_lens, split_chunk, out, lse,
                             stream);
 }
+
+// ---- no-allocation variant ---------------------------------------------------
+//
+// For callers that cannot allocate device memory: the split-KV partials live
+// in this file-scope array instead of a caller workspace.  Host code must not
+// pass the array's name to a kernel (in host code it names a host-side
+// stand-in); it passes the device address looked up below.
+
+static __device__ __align__(256) uint8_t g_static_scratch[K16V8_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+static int32_t static_scratch_address(void **ptr) {
+  static void *cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return K16V8_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && cached[dev]) {
+    *ptr = cached[dev];
+    return K16V8_OK;
+  }
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return K16V8_ERR_CUDA;
+  if (dev >= 0 && dev < 64) cached[dev] = p;
+  *ptr = p;
+  return K16V8_OK;
+}
+
+extern "C" int32_t k16v8_paged_decode_attention_static(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t max_seq_len, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, int32_t split_chunk, void *out,
+    float *lse, int32_t *dev_error, void *stream) {
+  const int32_t st0 = check_attention_shape(num_qo_heads, num_kv_heads, head_dim);
+  if (st0 != K16V8_OK) return st0;
+  const size_t need =
+      k16v8_decode_workspace_size(batch, num_qo_heads, head_dim, max_seq_len, split_chunk);
+  if (need == 0) return K16V8_ERR_INVALID_ARG;
+  if (need > K16V8_STATIC_SCRATCH_BYTES) return K16V8_ERR_STATIC_SCRATCH_LIMIT;
+  if (batch == 0) return K16V8_OK;
+  void *scratch = nullptr;
+  const int32_t st = static_scratch_address(&scratch);
+  if (st != K16V8_OK) return st;
+  return k16v8_paged_decode_attention(q, k_cache, v_cache, v_scale, block_table,
+                                      max_pages_per_seq, seq_lens, max_seq_len, batch,
+                                      num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale,
+                                      split_chunk, scratch, K16V8_STATIC_SCRATCH_BYTES, out, lse,
+                                      dev_error, stream);
+}

@@ -22,6 +22,8 @@ K16V8_ERR_UNSUPPORTED_SHAPE = 2
 K16V8_ERR_WORKSPACE_TOO_SMALL = 3
 K16V8_ERR_CUDA = 4
 K16V8_ERR_DEVICE_BOUNDS = 5
+K16V8_ERR_STATIC_SCRATCH_LIMIT = 6
+STATIC_SCRATCH_BYTES = 32 << 20
 K16V8_F16 = 0
 K16V8_F32 = 1
 DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 1, 2, 4, 8
@@ -44,6 +46,9 @@ SIGNATURES = {
     "k16v8_paged_decode_attention": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32,
                                             _i32, _i32, _i32, _f32, _i32, _P, _sz, _P, _P,
                                             _P, _P]),
+    "k16v8_paged_decode_attention_static": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32,
+                                                   _i32, _i32, _i32, _i32, _f32, _i32, _P, _P,
+                                                   _P, _P]),
     "k16v8_read_device_error": (_i32, [_P, _P, ctypes.POINTER(_i32)]),
     "k16v8_status_string": (ctypes.c_char_p, [_i32]),
 }
@@ -176,6 +181,22 @@ def k16v8_paged_decode_attention(q, k_cache, v_cache, v_scale, block_table, seq_
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _ptr(dev_error),
         _stream(stream))
     _check("k16v8_paged_decode_attention", st)
+
+
+def k16v8_paged_decode_attention_static(q, k_cache, v_cache, v_scale, block_table, seq_lens,
+                                        max_seq_len, sm_scale, split_chunk, out, lse=None,
+                                        dev_error=None, stream=None):
+    """Decode attention with the partials in the library's built-in device
+    scratch: for callers that cannot allocate device memory.  Calls that
+    overlap on the GPU race on that scratch; the first call on a device
+    should come before any stream capture."""
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_attention_static(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), int(max_seq_len), B, hq, k_cache.shape[1], d,
+        k_cache.shape[0], float(sm_scale), int(split_chunk), _ptr(out), _ptr(lse),
+        _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_decode_attention_static", st)
 
 
 def k16v8_read_device_error(dev_error, stream=None) -> int:

@@ -14,7 +14,8 @@
  * Conventions shared by every call
  *  - Pointers named as device pointers must point to device memory of the
  *    current device; the caller owns all memory.  The library allocates
- *    nothing and keeps no state between calls.
+ *    nothing and keeps no state between calls, apart from the built-in
+ *    scratch array of k16v8_paged_decode_attention_static.
  *  - Every launching call is asynchronous on `stream` (a cudaStream_t passed
  *    as void*; NULL is the legacy default stream).  Only
  *    k16v8_read_device_error synchronises.
@@ -56,7 +57,8 @@ typedef enum {
     K16V8_ERR_UNSUPPORTED_SHAPE = 2,  /* head_dim / GQA group not supported */
     K16V8_ERR_WORKSPACE_TOO_SMALL = 3,
     K16V8_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
-    K16V8_ERR_DEVICE_BOUNDS = 5       /* returned by k16v8_read_device_error */
+    K16V8_ERR_DEVICE_BOUNDS = 5,      /* returned by k16v8_read_device_error */
+    K16V8_ERR_STATIC_SCRATCH_LIMIT = 6 /* problem too large for the built-in scratch */
 } k16v8_status;
 
 typedef enum { K16V8_F16 = 0, K16V8_F32 = 1 } k16v8_dtype;
@@ -186,6 +188,38 @@ int32_t k16v8_paged_decode_attention(const void *q, const void *k_cache,
                                      int32_t split_chunk, void *workspace,
                                      size_t workspace_bytes, void *out, float *lse,
                                      int32_t *dev_error, void *stream);
+
+/*
+ * paged_decode_attention_static -- the same computation as
+ * k16v8_paged_decode_attention, for callers that cannot allocate device
+ * memory: a host that runs inside an engine whose memory manager owns every
+ * byte of the device, or code that must not call the CUDA allocator at all
+ * (hard real-time paths, plug-ins loaded into a process that forbids it).
+ * There is no counterpart in the paper; this is a packaging variant only.
+ *
+ * The split-KV partials go to a scratch array built into the library
+ * (K16V8_STATIC_SCRATCH_BYTES bytes of device memory that every GPU which
+ * loads the library keeps until the process exits) instead of a caller
+ * workspace.  The call allocates nothing.
+ *  - Needs k16v8_decode_workspace_size(batch, num_qo_heads, head_dim,
+ *    max_seq_len, split_chunk) <= K16V8_STATIC_SCRATCH_BYTES, else returns
+ *    K16V8_ERR_STATIC_SCRATCH_LIMIT and launches nothing.
+ *  - The first call on a device looks up that device's address of the
+ *    array (with the device current); make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array, and nothing in it needs to
+ *    start at zero (each call writes every partial it reads).  Calls whose
+ *    kernels overlap on the GPU (different streams, or concurrent host
+ *    threads) race on it: serialise them.
+ * Other arguments, layouts and errors as for k16v8_paged_decode_attention.
+ */
+#define K16V8_STATIC_SCRATCH_BYTES (32u << 20)
+int32_t k16v8_paged_decode_attention_static(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t max_seq_len, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, int32_t split_chunk, void *out,
+    float *lse, int32_t *dev_error, void *stream);
 
 /*
  * Wait for `stream`, then copy the device error word to *host_value and
