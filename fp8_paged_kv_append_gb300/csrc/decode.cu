@@ -15,15 +15,19 @@
 //    (page, KV head) are contiguous in the cache layout -- completing on an
 //    mbarrier; no register staging, no address arithmetic per element.
 //  * Q.K: eight lanes own one token (16 dims each, conflict-free 16-byte
-//    shared loads), fp32 FMAs against the pre-scaled query in registers,
-//    then a 3-step reduce-scatter so each lane ends with one (token, head)
-//    score: 4 shuffles per 4 tokens.
+//    shared loads), fp16-operand FMAs with fp32 accumulation against the
+//    query held as packed fp16 pairs, then a 3-step reduce-scatter so each
+//    lane ends with one (token, head) score: 4 shuffles per 4 tokens.
 //  * Online softmax in the log2 domain per page (running max / sum).
-//  * P.V: 16 lanes span the 128 dims (8 each), two tokens per step;
-//    E4M3 -> half2 -> fp32 dequant in registers; the per-head value scale is
-//    applied once to the final partial (it factors out of the sum).
+//  * P.V: each lane owns 4 dims of every token; E4M3 -> fp16 pairs by the
+//    hardware cvt, fp16x2 FMAs summed over one 16-token page (p <= 1 and
+//    |v| <= 448 keep a page sum below 7168), folded into fp32 state per
+//    page.  The per-head value scale is applied once to the final partial
+//    (it factors out of the sum).
 //  * The four warps' states are combined in shared memory; the CTA writes
 //    one fp32 partial row per query head plus its natural-log LSE.
+//  * Launched with programmatic stream serialization: griddepcontrol.wait
+//    precedes every read of inputs.
 #include <math.h>
 
 #include "k16v8_device.cuh"
