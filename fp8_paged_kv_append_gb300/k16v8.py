@@ -49,6 +49,9 @@ SIGNATURES = {
     "k16v8_paged_decode_attention_static": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32,
                                                    _i32, _i32, _i32, _i32, _f32, _i32, _P, _P,
                                                    _P, _P]),
+    "k16v8_paged_prefill_attention": (_i32, [_P, _P, _i32, _i32, _P, _P, _P, _P, _i32, _P,
+                                             _i32, _i32, _i32, _i32, _i32, _f32, _P, _P, _P,
+                                             _P]),
     "k16v8_read_device_error": (_i32, [_P, _P, ctypes.POINTER(_i32)]),
     "k16v8_status_string": (ctypes.c_char_p, [_i32]),
 }
@@ -181,6 +184,20 @@ def k16v8_paged_decode_attention(q, k_cache, v_cache, v_scale, block_table, seq_
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _ptr(dev_error),
         _stream(stream))
     _check("k16v8_paged_decode_attention", st)
+
+
+def k16v8_paged_prefill_attention(q, qo_indptr, max_qlen, k_cache, v_cache, v_scale,
+                                  block_table, seq_lens, sm_scale, out, lse=None, dev_error=None,
+                                  stream=None):
+    """Causal attention of q [total_q, Hq, D] (ragged by qo_indptr [B+1])
+    against the paged cache, whose seq_lens include these new tokens."""
+    total_q, hq, d = q.shape
+    st = load_library().k16v8_paged_prefill_attention(
+        _ptr(q), _ptr(qo_indptr), total_q, int(max_qlen), _ptr(k_cache), _ptr(v_cache),
+        _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        seq_lens.shape[0], hq, k_cache.shape[1], d, k_cache.shape[0], float(sm_scale), _ptr(out),
+        _ptr(lse), _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_prefill_attention", st)
 
 
 def k16v8_paged_decode_attention_static(q, k_cache, v_cache, v_scale, block_table, seq_lens,

@@ -190,6 +190,41 @@ int32_t k16v8_paged_decode_attention(const void *q, const void *k_cache,
                                      int32_t *dev_error, void *stream);
 
 /*
+ * paged_prefill_attention -- causal attention of a chunk of new prompt tokens
+ * against the paged cache, on tensor cores.  The page's throughput metric
+ * includes prefill ("Fixed throughput studies"); its 8K profile admits fresh
+ * prompts before batch-16 decode ("Matched diagnostic profiles").  The
+ * cache must already hold the chunk (call k16v8_kv_append first).
+ *
+ * Sequence b has qlen_b = qo_indptr[b+1] - qo_indptr[b] new tokens: the last
+ * qlen_b of its seq_lens[b] cached positions.  Query row i of that sequence
+ * sits at position p = seq_lens[b] - qlen_b + (i - qo_indptr[b]) and attends
+ * to positions 0..p (causal).  With s_j = sm_scale * q[i][h].k_j and
+ * v_j = v_scale[h/4] * e4m3(v8_j):
+ *   out[i][h][:] = sum_{j<=p} exp(s_j - lse) v_j,   lse[i][h] = ln sum_{j<=p} exp(s_j)
+ *
+ *   q           device fp16 [total_q][num_qo_heads][head_dim], 16-B aligned
+ *   qo_indptr   device int32 [batch+1], non-decreasing, qo_indptr[0] = 0,
+ *               qo_indptr[batch] = total_q
+ *   max_qlen    host hint: the largest qlen_b (sizes the grid)
+ *   block_table, seq_lens, caches, v_scale: as for decode
+ *   out         device fp16 [total_q][num_qo_heads][head_dim], 16-B aligned
+ *   lse         device fp32 [total_q][num_qo_heads] or NULL
+ * A sequence with qlen_b > seq_lens[b], seq_lens[b] > 16*max_pages_per_seq
+ * or rows outside [0, total_q) flags K16V8_DEVERR_SEQLEN and is skipped; page ids outside [0, num_pages)
+ * flag K16V8_DEVERR_PAGE and are not read.  No workspace is needed.
+ */
+int32_t k16v8_paged_prefill_attention(const void *q, const int32_t *qo_indptr,
+                                      int32_t total_q, int32_t max_qlen,
+                                      const void *k_cache, const uint8_t *v_cache,
+                                      const float *v_scale, const int32_t *block_table,
+                                      int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                      int32_t batch, int32_t num_qo_heads,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t num_pages, float sm_scale, void *out,
+                                      float *lse, int32_t *dev_error, void *stream);
+
+/*
  * paged_decode_attention_static -- the same computation as
  * k16v8_paged_decode_attention, for callers that cannot allocate device
  * memory: a host that runs inside an engine whose memory manager owns every

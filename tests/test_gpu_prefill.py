@@ -1,0 +1,96 @@
+"""Paged causal prefill on tensor cores against the oracle.
+
+The cache is written call by call by kv_append (as a chunked prefill does),
+then each call's queries attend to their prefix.  Tolerance as for decode:
+|out - ref| <= 4e-3 + 4e-3 |ref|, |lse - ref| <= 1e-4."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_paged_kv_append_gb300 import workloads
+from cases import check_close, dev, gpu_poisoned_caches, oracle_cache, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def K():
+    from fp8_paged_kv_append_gb300 import k16v8
+    k16v8.load_library()
+    return k16v8
+
+
+def run_calls(K, p, rows_to_check=None, err=None):
+    """Append + prefill for every call of a PrefillInputs; returns
+    {call index: (out, lse)} on the host."""
+    kc, vc = gpu_poisoned_caches(p.num_pages, p.num_kv_heads, p.head_dim)
+    vs = to_dev(p.v_scale)
+    res = []
+    for call in p.calls:
+        rows = call.rows
+        K.k16v8_kv_append(to_dev(p.k_tok[rows]), to_dev(p.v_tok[rows]),
+                          to_dev(p.slot_mapping[rows]), vs, kc, vc, err)
+        q = to_dev(p.q[rows])
+        out = torch.full(q.shape, float("nan"), dtype=torch.float16, device=dev())
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=dev())
+        K.k16v8_paged_prefill_attention(q, to_dev(call.qo_indptr), int(call.qlens.max()), kc, vc,
+                                        vs, to_dev(call.block_table), to_dev(call.seq_lens),
+                                        p.sm_scale, out, lse, err)
+        res.append((out.float().cpu().numpy(), lse.cpu().numpy()))
+    return res
+
+
+def check_against_oracle(p, res, sample=None):
+    okc, ovc = oracle_cache(p)
+    for ci, call in enumerate(p.calls):
+        o, l = res[ci]
+        rows = None
+        if sample is not None:
+            rows = np.unique(np.concatenate([np.arange(0, len(call.rows), sample),
+                                             call.qo_indptr[1:] - 1])).astype(np.int64)
+        ro, rl = oracle.paged_prefill(np.ascontiguousarray(p.q[call.rows]), call.qo_indptr, okc,
+                                      ovc, p.v_scale, call.block_table, call.seq_lens,
+                                      p.sm_scale, rows=rows)
+        if rows is not None:
+            o, l = o[rows], l[rows]
+        check_close(o, ro, l, rl)
+
+
+def test_prefill_small_ragged_chunks(K):
+    p = workloads.make_prefill("small", 7, [70, 33, 130, 1, 256], chunk=48, num_qo_heads=8,
+                               num_kv_heads=2)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    res = run_calls(K, p, err=err)
+    assert K.k16v8_read_device_error(err) == 0
+    check_against_oracle(p, res)
+
+
+def test_prefill_single_long_chunk_tile_edges(K):
+    # lengths around the 32-token query tile and 128-token KV tile edges
+    p = workloads.make_prefill("edges", 8, [31, 32, 33, 127, 128, 129, 300], chunk=1024,
+                               num_qo_heads=8, num_kv_heads=2)
+    res = run_calls(K, p)
+    check_against_oracle(p, res)
+
+
+def test_prefill_8x1k(K):
+    p = workloads.prefill_8x1k()
+    res = run_calls(K, p)
+    check_against_oracle(p, res)
+
+
+def test_prefill_1x8k_in_8_chunks_sampled(K):
+    p = workloads.prefill_1x8k()
+    res = run_calls(K, p)
+    check_against_oracle(p, res, sample=41)
+
+
+def test_prefill_bad_page_is_flagged(K):
+    p = workloads.make_prefill("bad", 9, [100], chunk=1024, num_qo_heads=8, num_kv_heads=2)
+    call = p.calls[0]
+    call.block_table = call.block_table.copy()
+    call.block_table[0, 2] = p.num_pages + 5
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    run_calls(K, p, err=err)
+    assert K.k16v8_read_device_error(err) & K.DEVERR_PAGE
