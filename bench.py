@@ -336,6 +336,103 @@ class DecodeBench:
         return dt, h2d, d2h
 
 
+# ---- chunked prefill on the GPU --------------------------------------------------
+
+def prefill_flops(p) -> float:
+    """Algorithmic flops of a prefill workload: 4 * D * Hq per visible
+    (query, key) pair (Q.K^T and P.V over the causal prefix)."""
+    pairs = 0
+    for call in p.calls:
+        for st, ql in zip(call.starts.tolist(), call.qlens.tolist()):
+            pairs += sum(st + i + 1 for i in range(ql))
+    return 4.0 * p.head_dim * p.num_qo_heads * pairs
+
+
+class PrefillBench:
+    """All calls of a chunked-prefill workload (per call: kv_append of the
+    chunk, then prefill attention), replayed from CUDA graphs."""
+
+    def __init__(self, p, device):
+        import torch
+        from fp8_paged_kv_append_gb300 import k16v8 as K
+        self.K, self.torch, self.p, self.dev = K, torch, p, device
+        td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.kc = torch.zeros((p.num_pages, p.num_kv_heads, 16, p.head_dim), dtype=torch.float16,
+                              device=device)
+        self.vc = torch.zeros((p.num_pages, p.num_kv_heads, 16, p.head_dim), dtype=torch.uint8,
+                              device=device)
+        self.vs = td(p.v_scale)
+        self.calls = []
+        for call in p.calls:
+            rows = call.rows
+            q = td(p.q[rows])
+            self.calls.append(dict(
+                k=td(p.k_tok[rows]), v=td(p.v_tok[rows]), slots=td(p.slot_mapping[rows]), q=q,
+                indptr=td(call.qo_indptr), bt=td(call.block_table), lens=td(call.seq_lens),
+                max_qlen=int(call.qlens.max()),
+                out=torch.empty(q.shape, dtype=torch.float16, device=device),
+                lse=torch.empty(q.shape[:2], dtype=torch.float32, device=device)))
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def append(self, c):
+        self.K.k16v8_kv_append(c["k"], c["v"], c["slots"], self.vs, self.kc, self.vc, self.err)
+
+    def attend(self, c):
+        self.K.k16v8_paged_prefill_attention(c["q"], c["indptr"], c["max_qlen"], self.kc, self.vc,
+                                             self.vs, c["bt"], c["lens"], self.p.sm_scale,
+                                             c["out"], c["lse"], self.err)
+
+    def step(self):
+        for c in self.calls:
+            self.append(c)
+            self.attend(c)
+
+    def _graph(self, fn, reps):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream(self.dev),
+                              capture_error_mode="thread_local"):
+            for _ in range(reps):
+                fn()
+        return g
+
+    def _time(self, g, reps_inside):
+        torch = self.torch
+        g.replay()
+        torch.cuda.synchronize(self.dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        g.replay()
+        t1.record()
+        torch.cuda.synchronize(self.dev)
+        return t0.elapsed_time(t1) / reps_inside
+
+    def run(self, steps, warmup):
+        torch = self.torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize(self.dev)
+        step_ms = self._time(self._graph(self.step, steps), steps)
+        attn_ms = self._time(self._graph(lambda: [self.attend(c) for c in self.calls], steps), steps)
+        app_ms = self._time(self._graph(lambda: [self.append(c) for c in self.calls], steps), steps)
+        if self.K.k16v8_read_device_error(self.err) != 0:
+            raise RuntimeError("device error flag raised during the prefill benchmark")
+        return step_ms, attn_ms, app_ms
+
+
+def prefill_line(p, device, steps, warmup, tensor_peak):
+    pb = PrefillBench(p, device)
+    step_ms, attn_ms, app_ms = pb.run(steps, warmup)
+    fl = prefill_flops(p)
+    return {"workload": p.name, "calls": len(p.calls), "query_tokens": int(p.q.shape[0]),
+            "ms_per_prompt_batch": round(step_ms, 4),
+            "prefill_attention_ms": round(attn_ms, 4), "kv_append_ms": round(app_ms, 4),
+            "algorithmic_tflop": round(fl / 1e12, 4),
+            "prefill_tflops": round(fl / (attn_ms * 1e-3) / 1e12, 1),
+            "frac_of_fp16_tensor_peak": round(fl / (attn_ms * 1e-3) / 1e12 / tensor_peak, 4)}
+
+
 # ---- CPU baseline: the oracle on the host cores -------------------------------------
 
 def oracle_decode_pass(w, okc, ovc, chunk, sample_b, nthreads):
@@ -401,7 +498,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="1k", choices=["1k", "8k"])
+    ap.add_argument("--workload", default="1k", choices=["1k", "8k", "prefill"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary 8K/b16 line inside the JSON")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -413,6 +510,8 @@ def main():
 
     if args.impl == "reference":
         return main_reference(args, rank, world)
+    if args.workload == "prefill":
+        return main_prefill(args)
 
     import torch
     import torch.distributed as dist
@@ -487,10 +586,35 @@ def main():
             "split_frac_of_hbm_peak": round(sb8 / (s8 * 1e-6) / 1e9 / hbm_peak, 4),
             "step_frac_of_hbm_peak": round(u8 / (t8 * 1e-3) / 1e9 / hbm_peak, 4),
             "config": config_of(w8, label8, chunk8, b8.R)}}
+    if not args.no_extra and args.workload == "1k":
+        from fp8_paged_kv_append_gb300 import workloads
+        _, tpeak, tkind = load_peaks()
+        torch.cuda.empty_cache()
+        line["extra"]["prefill"] = {
+            "peak_tflops": tpeak, "peak_kind": f"{tkind} dense bf16 (fp16 has the same nominal rate)",
+            "8x1024": prefill_line(workloads.prefill_8x1k(), device, 10, 3, tpeak),
+            "1x8192_in_8_chunks": prefill_line(workloads.prefill_1x8k(), device, 5, 2, tpeak)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def main_prefill(args):
+    """Prefill-only line (for profiling the tensor-core kernel)."""
+    import torch
+    from fp8_paged_kv_append_gb300 import k16v8 as K
+    from fp8_paged_kv_append_gb300 import workloads
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    K.load_library()
+    _, tpeak, tkind = load_peaks()
+    res = {"8x1024": prefill_line(workloads.prefill_8x1k(), device, args.steps,
+                                  max(3, args.warmup), tpeak)}
+    if not args.no_extra:
+        res["1x8192_in_8_chunks"] = prefill_line(workloads.prefill_1x8k(), device, args.steps,
+                                                 max(3, args.warmup), tpeak)
+    print(json.dumps({"prefill": res, "peak_tflops": tpeak, "peak_kind": tkind}), flush=True)
 
 
 def main_reference(args, rank, world):
