@@ -12,14 +12,16 @@
 // (row = token*4 + head), so every K/V tile loaded serves 4 heads.
 //  * Q tile: one TMA box (64 dims x 4 heads x 32 tokens, 128-byte swizzle)
 //    per half of the head dimension; loaded once.
-//  * K tile (128 positions = 8 pages): per page and half, one TMA box of the
+//  * K tile (64 positions = 4 pages): per page and half, one TMA box of the
 //    (page, head) rows straight into the K-major SW128 operand layout;
 //    double-buffered.
-//  * V tile: the 8 E4M3 pages by bulk copy, then dequantised by the CTA's
+//  * V tile: the 4 E4M3 pages by bulk copy, then dequantised by the CTA's
 //    threads (hardware E4M3 -> fp16 cvt) into an MN-major SW128 operand.
-//  * S = Q K^T and O += P V are tcgen05.mma kind::f16 (M 128, N 128, K 16
-//    per instruction) issued by one thread, accumulating in tensor memory
-//    (S: 128 columns, O: 128 columns).
+//  * S = Q K^T (M 128, N 64) and O += P V (M 128, N 128) are tcgen05.mma
+//    kind::f16 (K 16 per instruction) issued by one thread, accumulating in
+//    tensor memory (S: 64 columns, O: 128 columns).  112 KB of shared memory
+//    and 256 tensor-memory columns per CTA let two CTAs share an SM, so one
+//    CTA's softmax overlaps the other's MMAs.
 //  * Softmax: thread r owns row r: it loads its S row from tensor memory,
 //    applies the causal mask and the log2-domain scale, keeps a running max
 //    (the O row is rescaled in tensor memory only when the max grows by more
@@ -39,18 +41,22 @@ namespace prefill {
 
 constexpr int kQTok = 32;                  // query tokens per tile
 constexpr int kRows = kQTok * kGroup;      // 128 MMA rows
-constexpr int kKv = 128;                   // KV positions per tile
-constexpr int kPagesPerTile = kKv / kPage; // 8
+constexpr int kKv = 64;                    // KV positions per tile
+constexpr int kPagesPerTile = kKv / kPage; // 4
 constexpr int kThreads = 128;
 
-constexpr uint32_t kOffQ = 0;                      // 2 x [128][64] fp16
-constexpr uint32_t kOffK = 32768;                  // 2 stages x 2 x [128][64] fp16
-constexpr uint32_t kOffVst = kOffK + 2 * 32768;    // 2 stages x [128][128] E4M3
-constexpr uint32_t kOffV = kOffVst + 2 * 16384;    // 2 MN blocks x [128 pos][64] fp16
-constexpr uint32_t kOffP = kOffV + 32768;          // 2 K blocks x [128 rows][64] fp16
-constexpr uint32_t kOffBar = kOffP + 32768;        // mbarriers + tmem slot
-constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 256;                // S [0,128), O [128,256)
+// Shared memory (112 KB + barriers: two CTAs per SM).  Operand tiles start
+// on 1024-byte boundaries (the dynamic shared window is 1024-aligned; the
+// kernel checks).
+constexpr uint32_t kKBlk = kKv * 128;              // one 64-dim half of a K tile
+constexpr uint32_t kOffQ = 0;                      // 2 K-blocks x [128 rows][64] fp16
+constexpr uint32_t kOffK = 32768;                  // 2 stages x 2 K-blocks x [64 pos][64]
+constexpr uint32_t kOffVst = kOffK + 2 * 2 * kKBlk;    // 2 stages x [64 pos][128] E4M3
+constexpr uint32_t kOffV = kOffVst + 2 * kKv * 128;    // 2 MN-blocks x [64 pos][64] fp16
+constexpr uint32_t kOffP = kOffV + 2 * kKBlk;          // 1 K-block x [128 rows][64] fp16
+constexpr uint32_t kOffBar = kOffP + kRows * 128;      // mbarriers, tmem slot, abort flag
+constexpr uint32_t kSmemBytes = kOffBar + 128;
+constexpr uint32_t kTmemCols = 256;                // S [0,64), O [128,256)
 
 enum { kBarQ = 0, kBarKv0 = 1, kBarKv1 = 2, kBarS = 3, kBarPv = 4 };
 
@@ -67,16 +73,15 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, volatil
   return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
+__global__ void __launch_bounds__(kThreads, 2) prefill_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const uint8_t *__restrict__ v_cache, const float *__restrict__ v_scale,
     const int32_t *__restrict__ qo_indptr, const int32_t *__restrict__ block_table, int32_t maxp,
     const int32_t *__restrict__ seq_lens, int32_t total_q, int32_t hq, int32_t hkv,
     int32_t num_pages, float sm_scale, __half *__restrict__ out, float *__restrict__ lse_out,
     int32_t *dev_error) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *base = smem_raw;
   uint8_t *sQ = base + kOffQ;
   uint8_t *sK = base + kOffK;
   uint8_t *sVst = base + kOffVst;
@@ -90,6 +95,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   const int g = blockIdx.y, b = blockIdx.z;
   const int tile = gridDim.x - 1 - blockIdx.x;  // longest (latest) tiles first
   pdl_wait();
+  if (smem_addr(smem_raw) & 1023u) {  // operand tiles need 1024-byte alignment
+    if (tid == 0) flag_error(dev_error, K16V8_DEVERR_INTERNAL);
+    return;
+  }
 
   const int q0 = __ldg(qo_indptr + b);
   const int qlen = __ldg(qo_indptr + b + 1) - q0;
@@ -126,34 +135,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   auto load_kv = [&](int j) {
     const int s = j & 1;
     uint64_t *bar = &bars[kBarKv0 + s];
-    int pid[kPagesPerTile];
-    uint32_t bytes = 0;
     const int first_page = j * kPagesPerTile;
     const int live_pages = min(kPagesPerTile, (L - j * kKv + kPage - 1) / kPage);
-#pragma unroll
-    for (int i = 0; i < kPagesPerTile; ++i) {
-      pid[i] = -1;
-      if (i < live_pages) {
-        int p = __ldg(bt + first_page + i);
-        if (p < 0 || p >= num_pages) {
-          flag_error(dev_error, K16V8_DEVERR_PAGE);
-          p = -1;
-        }
-        pid[i] = p;
-        if (p >= 0) bytes += 2 * 2048 + 2048;
+    int pid0 = -1, pid1 = -1, pid2 = -1, pid3 = -1;
+    uint32_t bytes = 0;
+    auto get = [&](int i) {
+      if (i >= live_pages) return -1;
+      int p = __ldg(bt + first_page + i);
+      if (p < 0 || p >= num_pages) {
+        flag_error(dev_error, K16V8_DEVERR_PAGE);
+        return -1;
       }
-    }
+      bytes += 3 * 2048;
+      return p;
+    };
+    pid0 = get(0);
+    pid1 = get(1);
+    pid2 = get(2);
+    pid3 = get(3);
     mbar_arrive_expect_tx(bar, bytes);
-    uint8_t *k_dst = sK + s * 32768;
-    uint8_t *v_dst = sVst + s * 16384;
-#pragma unroll
-    for (int i = 0; i < kPagesPerTile; ++i) {
-      if (pid[i] < 0) continue;
-      const int row = (pid[i] * hkv + g) * kPage;
+    uint8_t *k_dst = sK + s * 2 * kKBlk;
+    uint8_t *v_dst = sVst + s * kKv * 128;
+    auto issue = [&](int i, int pid) {
+      if (pid < 0) return;
+      const int row = (pid * hkv + g) * kPage;
       tc::tma_load_2d(k_dst + i * 2048, &tmap_k, 0, row, bar);
-      tc::tma_load_2d(k_dst + 16384 + i * 2048, &tmap_k, 64, row, bar);
+      tc::tma_load_2d(k_dst + kKBlk + i * 2048, &tmap_k, 64, row, bar);
       bulk_g2s(v_dst + i * 2048, v_cache + static_cast<int64_t>(row) * kHeadDim, 2048, bar);
-    }
+    };
+    issue(0, pid0);
+    issue(1, pid1);
+    issue(2, pid2);
+    issue(3, pid3);
   };
 
   if (tid == 0) {
@@ -190,13 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                       cta_wait(&bars[kBarKv0 + s], kv_par, abort_flag, dev_error);
       if (ok) {
         tc::fence_after_sync();
-        const uint8_t *k_st = sK + s * 32768;
+        const uint8_t *k_st = sK + s * 2 * kKBlk;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad =
               tc::smem_desc_sw128(smem_addr(sQ + (kk >> 2) * 16384 + (kk & 3) * 32), 16, 1024);
           const uint64_t bd =
-              tc::smem_desc_sw128(smem_addr(k_st + (kk >> 2) * 16384 + (kk & 3) * 32), 16, 1024);
+              tc::smem_desc_sw128(smem_addr(k_st + (kk >> 2) * kKBlk + (kk & 3) * 32), 16, 1024);
           tc::mma_f16_ss(tS, ad, bd, kIdescQK, kk > 0);
         }
       }
@@ -208,10 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     // ---- dequantise V tile j into the MN-major fp16 operand ----
     cta_wait(&bars[kBarKv0 + s], kv_par, abort_flag, dev_error);
     {
-      const uint8_t *vst = sVst + s * 16384;
+      const uint8_t *vst = sVst + s * kKv * 128;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int id = tid + kThreads * i;  // 1024 chunks of 16 E4M3 values
+      for (int i = 0; i < kKv * 8 / kThreads; ++i) {
+        const int id = tid + kThreads * i;  // chunks of 16 E4M3 values
         const int pos = id >> 3, c16 = id & 7;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (j * kKv + pos < L) {
@@ -229,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           hi = make_uint4(hv[4], hv[5], hv[6], hv[7]);
         }
         const uint32_t off = pos * 128 + (c16 & 3) * 32;
-        uint8_t *blk = sV + (c16 >> 2) * 16384;
+        uint8_t *blk = sV + (c16 >> 2) * kKBlk;
         *reinterpret_cast<uint4 *>(blk + tc::sw128(off)) = lo;
         *reinterpret_cast<uint4 *>(blk + tc::sw128(off + 16)) = hi;
       }
@@ -238,19 +251,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     // ---- softmax of this thread's row ----
     cta_wait(&bars[kBarS], j & 1, abort_flag, dev_error);
     tc::fence_after_sync();
-    // pass 1: row max of the scaled, masked scores (32 columns at a time)
+    // pass 1: row max of the scaled, masked scores
     const bool need_mask = j * kKv + kKv - 1 > p_lo;
     const int lim = p_r - j * kKv;  // last visible column of this tile
     float rmax = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t sr[32];
-      tc::tmem_ld32(tS + lane_base + c * 32, sr);
+    {
+      uint32_t sa[32], sb[32];
+      tc::tmem_ld32(tS + lane_base, sa);
+      tc::tmem_ld32(tS + lane_base + 32, sb);
       tc::tmem_wait_ld();
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float v = __uint_as_float(sr[e]);
-        if (!need_mask || c * 32 + e <= lim) rmax = fmaxf(rmax, v);
+        if (!need_mask || e <= lim) rmax = fmaxf(rmax, __uint_as_float(sa[e]));
+        if (!need_mask || 32 + e <= lim) rmax = fmaxf(rmax, __uint_as_float(sb[e]));
       }
     }
     rmax *= qk_scale;
@@ -274,29 +287,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
     // pass 2: p = 2^(s*scale - m), fp16 into the P operand tile
     float psum = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t sr[32];
-      tc::tmem_ld32(tS + lane_base + c * 32, sr);
+    {
+      uint32_t sr[2][32];
+      tc::tmem_ld32(tS + lane_base, sr[0]);
+      tc::tmem_ld32(tS + lane_base + 32, sr[1]);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {  // 8 values -> one 16-byte chunk of P
-        uint32_t pk[4];
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c0 = c * 32 + q * 8 + 2 * e;
-          float p0 = ex2(fmaf(__uint_as_float(sr[q * 8 + 2 * e]), qk_scale, -m_used));
-          float p1 = ex2(fmaf(__uint_as_float(sr[q * 8 + 2 * e + 1]), qk_scale, -m_used));
-          if (need_mask && c0 > lim) p0 = 0.f;
-          if (need_mask && c0 + 1 > lim) p1 = 0.f;
-          psum += p0 + p1;
-          const __half2 h = __floats2half2_rn(p0, p1);
-          pk[e] = *reinterpret_cast<const uint32_t *>(&h);
+        for (int q = 0; q < 4; ++q) {  // 8 values -> one 16-byte chunk of P
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c0 = c * 32 + q * 8 + 2 * e;
+            float p0 = ex2(fmaf(__uint_as_float(sr[c][q * 8 + 2 * e]), qk_scale, -m_used));
+            float p1 = ex2(fmaf(__uint_as_float(sr[c][q * 8 + 2 * e + 1]), qk_scale, -m_used));
+            if (need_mask && c0 > lim) p0 = 0.f;
+            if (need_mask && c0 + 1 > lim) p1 = 0.f;
+            psum += p0 + p1;
+            const __half2 h = __floats2half2_rn(p0, p1);
+            pk[e] = *reinterpret_cast<const uint32_t *>(&h);
+          }
+          const uint32_t off = r * 128 + (c * 32 + q * 8) * 2;
+          *reinterpret_cast<uint4 *>(sP + tc::sw128(off)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        const int col = c * 32 + q * 8;  // first KV column of this chunk
-        const uint32_t off = r * 128 + (col & 63) * 2;
-        *reinterpret_cast<uint4 *>(sP + (col >> 6) * 16384 + tc::sw128(off)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
     l = l * alpha + psum;
@@ -308,10 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     if (tid == 0) {
       tc::fence_after_sync();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad =
-            tc::smem_desc_sw128(smem_addr(sP + (kk >> 2) * 16384 + (kk & 3) * 32), 16, 1024);
-        const uint64_t bd = tc::smem_desc_sw128(smem_addr(sV + kk * 2048), 16384, 1024);
+      for (int kk = 0; kk < kKv / 16; ++kk) {
+        const uint64_t ad = tc::smem_desc_sw128(smem_addr(sP + kk * 32), 16, 1024);
+        const uint64_t bd = tc::smem_desc_sw128(smem_addr(sV + kk * 2048), kKBlk, 1024);
         tc::mma_f16_ss(tO, ad, bd, kIdescPV, j > 0 || kk > 0);
       }
       tc::mma_commit(&bars[kBarPv]);

@@ -26,7 +26,7 @@ K16V8_ERR_STATIC_SCRATCH_LIMIT = 6
 STATIC_SCRATCH_BYTES = 32 << 20
 K16V8_F16 = 0
 K16V8_F32 = 1
-DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8, 16
 PAGE_SIZE = 16
 HEAD_DIM = 128
 

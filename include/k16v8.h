@@ -68,6 +68,7 @@ typedef enum { K16V8_F16 = 0, K16V8_F32 = 1 } k16v8_dtype;
 #define K16V8_DEVERR_PAGE 0x2    /* block_table entry outside [0, num_pages) */
 #define K16V8_DEVERR_SEQLEN 0x4  /* seq_len < 0, > max_seq_len, or > 16*max_pages_per_seq */
 #define K16V8_DEVERR_TIMEOUT 0x8 /* a bounded wait on an async copy gave up */
+#define K16V8_DEVERR_INTERNAL 0x10 /* a kernel's own layout check failed; nothing was written */
 
 /*
  * kv_append -- "the candidate also gathers values and writes the compressed
