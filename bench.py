@@ -433,6 +433,60 @@ def prefill_line(p, device, steps, warmup, tensor_peak):
             "frac_of_fp16_tensor_peak": round(fl / (attn_ms * 1e-3) / 1e12 / tensor_peak, 4)}
 
 
+# ---- full-pool ragged decode across 40 layers ------------------------------------
+
+def fullpool_line(device, steps, warmup, hbm_peak, layers=40):
+    """One decode step through all layers' attention (per layer: append the new
+    token, split-KV attention, merge) over 32 GiB of pools, replayed as one
+    CUDA graph."""
+    import torch
+    from fp8_paged_kv_append_gb300 import workloads
+    from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
+    lay = workloads.fullpool_layout(seed=4)
+    P, B = lay.num_pages, len(lay.seq_lens)
+    pools = [workloads.device_layer_pool(1000 + l, P, device) for l in range(layers)]
+    g = torch.Generator(device=device)
+    g.manual_seed(44)
+    qs = [torch.randn((B, 40, 128), generator=g, device=device, dtype=torch.float16)
+          for _ in range(layers)]
+    kn = [torch.randn((B, 10, 128), generator=g, device=device, dtype=torch.float16)
+          for _ in range(layers)]
+    vn = [torch.randn((B, 10, 128), generator=g, device=device, dtype=torch.float16)
+          for _ in range(layers)]
+    L = lay.seq_lens.astype(np.int64)
+    slots = lay.block_table[np.arange(B), (L - 1) // 16].astype(np.int64) * 16 + (L - 1) % 16
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    step = MultiLayerDecode([p[0] for p in pools], [p[1] for p in pools], [p[2] for p in pools],
+                            td(lay.block_table), td(lay.seq_lens), td(slots), int(L.max()), 40,
+                            split_chunk=512)
+    outs = [torch.empty((B, 40, 128), dtype=torch.float16, device=device) for _ in range(layers)]
+    lses = [torch.empty((B, 40), dtype=torch.float32, device=device) for _ in range(layers)]
+    step.capture(qs, kn, vn, outs, lses)
+    for _ in range(warmup):
+        step.replay()
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step.replay()
+    t1.record()
+    torch.cuda.synchronize(device)
+    if step.check() != 0:
+        raise RuntimeError("device error flag raised during the full-pool benchmark")
+    ms = t0.elapsed_time(t1) / steps
+    kvb = layers * int(L.sum()) * 10 * 128 * 3
+    del pools, step
+    torch.cuda.empty_cache()
+    return {"workload": f"full pool: {layers} layers x {P} pages (223,696 slots, 32 GiB), batch "
+                        f"{B}, seq_lens {int(L.min())}..{int(L.max())} (sum {int(L.sum())}, "
+                        f"{lay.draws} draw(s)), split 512, one CUDA graph per step",
+            "ms_per_step": round(ms, 4), "us_per_layer_step": round(ms * 1e3 / layers, 2),
+            "kv_bytes_per_step": kvb, "value": round(kvb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "gpu_launches_per_step": 3 * layers}
+
+
 # ---- CPU baseline: the oracle on the host cores -------------------------------------
 
 def oracle_decode_pass(w, okc, ovc, chunk, sample_b, nthreads):
@@ -498,7 +552,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="1k", choices=["1k", "8k", "prefill"])
+    ap.add_argument("--workload", default="1k", choices=["1k", "8k", "prefill", "fullpool"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary 8K/b16 line inside the JSON")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -512,6 +566,14 @@ def main():
         return main_reference(args, rank, world)
     if args.workload == "prefill":
         return main_prefill(args)
+    if args.workload == "fullpool":
+        import torch
+        from fp8_paged_kv_append_gb300 import k16v8 as K
+        torch.cuda.set_device(0)
+        K.load_library()
+        print(json.dumps({"fullpool_40_layers": fullpool_line(
+            torch.device("cuda", 0), args.steps, max(3, args.warmup), load_peaks()[0])}))
+        return
 
     import torch
     import torch.distributed as dist
@@ -588,6 +650,8 @@ def main():
             "config": config_of(w8, label8, chunk8, b8.R)}}
     if not args.no_extra and args.workload == "1k":
         from fp8_paged_kv_append_gb300 import workloads
+        torch.cuda.empty_cache()
+        line["extra"]["fullpool_40_layers"] = fullpool_line(device, 10, 3, hbm_peak)
         _, tpeak, tkind = load_peaks()
         torch.cuda.empty_cache()
         line["extra"]["prefill"] = {

@@ -1,0 +1,100 @@
+"""A whole-model decode step: kv_append + split-KV attention + LSE merge for
+every layer, replayed as one CUDA graph.
+
+The per-layer pools, scales and workspaces stay resident; a step takes each
+layer's new-token K/V and query and writes each layer's attention output.
+The value scales are checked on the host before the graph is captured (the
+subject page's production checks verify calibrated scales inside the engine
+before graph capture: "Phi-4: quality transfer and interrupted throughput
+studies", intro).  All computation runs in libk16v8's kernels; this module
+only sequences the calls and owns the graph.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import k16v8 as K
+
+
+class ScaleError(ValueError):
+    pass
+
+
+def validate_scales(v_scales) -> None:
+    """Every per-(layer, KV head) value scale must be finite and > 0."""
+    for li, s in enumerate(v_scales):
+        host = s.detach().float().cpu()
+        bad = ~(torch.isfinite(host) & (host > 0))
+        if bool(bad.any()):
+            idx = bad.nonzero().flatten().tolist()
+            raise ScaleError(f"layer {li}: value scale not finite and positive at KV heads {idx}")
+
+
+class MultiLayerDecode:
+    """Decode step over `len(k_caches)` layers that share one page table.
+
+    k_caches[l] fp16 [P,Hkv,16,D], v_caches[l] uint8 [P,Hkv,16,D], v_scales[l]
+    fp32 [Hkv]; block_table int32 [B, max_pages]; seq_lens int32 [B] (the
+    lengths after this step's append); slots int64 [B] (where the new token
+    of each sequence goes)."""
+
+    def __init__(self, k_caches, v_caches, v_scales, block_table, seq_lens, slots, max_seq_len,
+                 num_qo_heads, sm_scale=None, split_chunk=512, validate=True):
+        if validate:
+            validate_scales(v_scales)
+        self.k_caches, self.v_caches, self.v_scales = k_caches, v_caches, v_scales
+        self.block_table, self.seq_lens, self.slots = block_table, seq_lens, slots
+        self.max_seq_len = int(max_seq_len)
+        self.layers = len(k_caches)
+        dev = k_caches[0].device
+        self.batch = int(block_table.shape[0])
+        self.hq = int(num_qo_heads)
+        self.hkv = int(k_caches[0].shape[1])
+        self.d = int(k_caches[0].shape[3])
+        self.sm_scale = float(sm_scale if sm_scale is not None else 1.0 / math.sqrt(self.d))
+        self.chunk = int(split_chunk)
+        n = K.k16v8_decode_workspace_size(self.batch, self.hq, self.d, self.max_seq_len,
+                                          self.chunk)
+        if n == 0:
+            raise ValueError("invalid decode workspace shape")
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.partial_o, self.partial_lse = K.workspace_views(
+            self.workspace, self.batch, self.hq, self.d, self.max_seq_len, self.chunk)
+        self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
+
+    def layer(self, li, q, k_new, v_new, out, lse=None):
+        K.k16v8_kv_append(k_new, v_new, self.slots, self.v_scales[li], self.k_caches[li],
+                          self.v_caches[li], self.dev_error)
+        K.k16v8_paged_decode_split(q, self.k_caches[li], self.v_caches[li], self.v_scales[li],
+                                   self.block_table, self.seq_lens, self.max_seq_len,
+                                   self.sm_scale, self.chunk, self.workspace, self.dev_error)
+        K.k16v8_merge_states(self.partial_o, self.partial_lse, self.seq_lens, self.chunk, out,
+                             lse)
+
+    def step(self, qs, k_news, v_news, outs, lses=None):
+        for li in range(self.layers):
+            self.layer(li, qs[li], k_news[li], v_news[li], outs[li],
+                       None if lses is None else lses[li])
+
+    def capture(self, qs, k_news, v_news, outs, lses=None):
+        """Capture one whole step into a CUDA graph over these buffers (the
+        caller refills qs / k_news / v_news in place between replays)."""
+        self.step(qs, k_news, v_news, outs, lses)  # eager run configures the kernels
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream(), capture_error_mode="thread_local"):
+            self.step(qs, k_news, v_news, outs, lses)
+        self.graph = g
+        return g
+
+    def replay(self):
+        if self.graph is None:
+            raise RuntimeError("capture() first")
+        self.graph.replay()
+
+    def check(self) -> int:
+        """Synchronise and return the device error word (0 = clean)."""
+        return K.k16v8_read_device_error(self.dev_error)

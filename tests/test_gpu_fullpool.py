@@ -1,0 +1,103 @@
+"""Full-pool ragged decode across 40 layers (32 GiB of K16/V8 pools, 223,696
+slots per layer, batch 64 with lengths in [1, 8192]) through the graph-captured
+multi-layer step, checked against the oracle on sampled (layer, sequence)
+pairs.  The pools are drawn on the device with torch; the sampled sequences'
+pages are copied to the host before the step, and the oracle appends the new
+token itself, so no oracle input comes from the CUDA path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_paged_kv_append_gb300 import workloads
+from cases import check_close, dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+LAYERS = 40
+
+
+@pytest.fixture(scope="module")
+def setup():
+    from fp8_paged_kv_append_gb300 import k16v8 as K
+    from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
+    K.load_library()
+    lay = workloads.fullpool_layout(seed=4)
+    P, B = lay.num_pages, len(lay.seq_lens)
+    assert P * 16 == 223696 and int(np.sum(-(-lay.seq_lens // 16))) <= P
+    pools = [workloads.device_layer_pool(1000 + l, P, dev()) for l in range(LAYERS)]
+    rng = np.random.Generator(np.random.PCG64(44))
+    qs = [to_dev(rng.standard_normal((B, 40, 128), dtype=np.float32).astype(np.float16))
+          for _ in range(LAYERS)]
+    kn = [to_dev(rng.standard_normal((B, 10, 128), dtype=np.float32).astype(np.float16))
+          for _ in range(LAYERS)]
+    vn = [to_dev(rng.standard_normal((B, 10, 128), dtype=np.float32).astype(np.float16))
+          for _ in range(LAYERS)]
+    L = lay.seq_lens.astype(np.int64)
+    slots = (lay.block_table[np.arange(B), (L - 1) // 16].astype(np.int64) * 16 + (L - 1) % 16)
+    # host copies of the sampled sequences' pages, taken before any kernel runs
+    order = np.argsort(L)
+    seqs = sorted({int(order[0]), int(order[-1]), int(order[B // 2]), 5, 40})
+    sample = [(l, b) for l in (0, 17, 39) for b in seqs]
+    host = {}
+    for l, b in sample:
+        n = -(-int(L[b]) // 16)
+        pages = torch.from_numpy(lay.block_table[b, :n].astype(np.int64)).to(dev())
+        host[(l, b)] = (pools[l][0][pages].cpu().numpy(), pools[l][1][pages].cpu().numpy(),
+                        pools[l][2].cpu().numpy())
+    step = MultiLayerDecode([p[0] for p in pools], [p[1] for p in pools], [p[2] for p in pools],
+                            to_dev(lay.block_table), to_dev(lay.seq_lens), to_dev(slots),
+                            int(L.max()), 40, split_chunk=512)
+    outs = [torch.empty((B, 40, 128), dtype=torch.float16, device=dev()) for _ in range(LAYERS)]
+    lses = [torch.empty((B, 40), dtype=torch.float32, device=dev()) for _ in range(LAYERS)]
+    return dict(K=K, lay=lay, pools=pools, qs=qs, kn=kn, vn=vn, slots=slots, sample=sample,
+                host=host, step=step, outs=outs, lses=lses)
+
+
+def oracle_for(s, l, b):
+    kc, vc, vs = s["host"][(l, b)]
+    L = int(s["lay"].seq_lens[b])
+    kc, vc = kc.copy(), vc.copy()
+    pos = L - 1
+    slot = np.array([(pos // 16) * 16 + pos % 16], np.int64)  # compact page numbering
+    oracle.kv_append(s["kn"][l][b:b + 1].cpu().numpy(), s["vn"][l][b:b + 1].cpu().numpy(), slot, vs,
+                     kc, vc)
+    bt = np.arange(kc.shape[0], dtype=np.int32)[None, :]
+    q = s["qs"][l][b:b + 1].cpu().numpy()
+    r = oracle.paged_decode(q, kc, vc, vs, bt, np.array([L], np.int32), s["step"].sm_scale)
+    return r["out"][0], r["lse"][0]
+
+
+def test_fullpool_eager_step_matches_oracle(setup):
+    s = setup
+    s["step"].step(s["qs"], s["kn"], s["vn"], s["outs"], s["lses"])
+    assert s["step"].check() == 0
+    for l, b in s["sample"]:
+        ro, rl = oracle_for(s, l, b)
+        check_close(s["outs"][l][b].float().cpu().numpy(), ro, s["lses"][l][b].cpu().numpy(), rl)
+
+
+def test_fullpool_graph_replay_matches_eager(setup):
+    s = setup
+    ref = [o.clone() for o in s["outs"]]
+    ref_l = [x.clone() for x in s["lses"]]
+    for o in s["outs"]:
+        o.fill_(float("nan"))
+    s["step"].capture(s["qs"], s["kn"], s["vn"], s["outs"], s["lses"])
+    for o in s["outs"]:
+        o.fill_(float("nan"))
+    s["step"].replay()
+    assert s["step"].check() == 0
+    for l in range(LAYERS):
+        assert torch.equal(s["outs"][l], ref[l]) and torch.equal(s["lses"][l], ref_l[l])
+
+
+def test_scale_validation_rejects_bad_scale(setup):
+    from fp8_paged_kv_append_gb300.decode_step import ScaleError, validate_scales
+    bad = [p[2].clone() for p in setup["pools"][:2]]
+    bad[1][3] = float("nan")
+    with pytest.raises(ScaleError):
+        validate_scales(bad)
+    bad[1][3] = 0.0
+    with pytest.raises(ScaleError):
+        validate_scales(bad)
