@@ -150,11 +150,12 @@ def kv_bytes(w) -> int:
 class DecodeBench:
     """Device state for timed decode steps over `replicas` copies of the pool."""
 
-    def __init__(self, w, device, split_chunk=512, replicas=None):
+    def __init__(self, w, device, split_chunk=512, replicas=None, fused=False):
         import torch
         from fp8_paged_kv_append_gb300 import k16v8 as K
         self.K, self.torch, self.w, self.dev = K, torch, w, device
         self.chunk = split_chunk
+        self.fused = fused
         pool_bytes = w.num_pages * w.num_kv_heads * 16 * w.head_dim * 3
         self.R = replicas or max(1, -(-4 * L2_BYTES // pool_bytes))
         P = w.num_pages
@@ -176,6 +177,8 @@ class DecodeBench:
         del k_all, v_all
         self.k_new = td(w.k_tok[w.new_rows])
         self.v_new = td(w.v_tok[w.new_rows])
+        self.k_new16 = self.k_new.contiguous()
+        self.v_new16 = self.v_new.to(torch.float16).contiguous()
         self.q = td(w.q)
         self.seq_lens = td(w.seq_lens)
         self.max_len = int(w.seq_lens.max())
@@ -191,13 +194,20 @@ class DecodeBench:
         K, r = self.K, i % self.R
         if ev:
             ev[0].record()
-        K.k16v8_kv_append(self.k_new, self.v_new, self.slots_new[r], self.v_scale, self.kc,
-                          self.vc, self.err)
+        if not self.fused:
+            K.k16v8_kv_append(self.k_new, self.v_new, self.slots_new[r], self.v_scale, self.kc,
+                              self.vc, self.err)
         if ev:
             ev[1].record()
-        K.k16v8_paged_decode_split(self.q, self.kc, self.vc, self.v_scale, self.bt[r],
-                                   self.seq_lens, self.max_len, self.w.sm_scale, self.chunk,
-                                   self.ws, self.err)
+        if self.fused:
+            K.k16v8_paged_decode_append_split(self.q, self.k_new16, self.v_new16, self.kc, self.vc,
+                                              self.v_scale, self.bt[r], self.seq_lens,
+                                              self.max_len, self.w.sm_scale, self.chunk, self.ws,
+                                              self.err)
+        else:
+            K.k16v8_paged_decode_split(self.q, self.kc, self.vc, self.v_scale, self.bt[r],
+                                       self.seq_lens, self.max_len, self.w.sm_scale, self.chunk,
+                                       self.ws, self.err)
         if ev:
             ev[2].record()
         K.k16v8_merge_states(self.po, self.pl, self.seq_lens, self.chunk, self.out, self.lse)
@@ -254,17 +264,26 @@ class DecodeBench:
         `steps` launches (rotating over the pool replicas), timed as a block."""
         torch, K = self.torch, self.K
         outs = []
+        split = (lambda i: K.k16v8_paged_decode_append_split(
+                     self.q, self.k_new16, self.v_new16, self.kc, self.vc, self.v_scale,
+                     self.bt[i % self.R], self.seq_lens, self.max_len, self.w.sm_scale,
+                     self.chunk, self.ws, self.err)) if self.fused else (
+                 lambda i: K.k16v8_paged_decode_split(self.q, self.kc, self.vc, self.v_scale,
+                                                      self.bt[i % self.R], self.seq_lens,
+                                                      self.max_len, self.w.sm_scale, self.chunk,
+                                                      self.ws, self.err))
         kinds = [
-            lambda i: K.k16v8_kv_append(self.k_new, self.v_new, self.slots_new[i % self.R],
-                                        self.v_scale, self.kc, self.vc, self.err),
-            lambda i: K.k16v8_paged_decode_split(self.q, self.kc, self.vc, self.v_scale,
-                                                 self.bt[i % self.R], self.seq_lens,
-                                                 self.max_len, self.w.sm_scale, self.chunk,
-                                                 self.ws, self.err),
+            (lambda i: None) if self.fused else (
+                lambda i: K.k16v8_kv_append(self.k_new, self.v_new, self.slots_new[i % self.R],
+                                            self.v_scale, self.kc, self.vc, self.err)),
+            split,
             lambda i: K.k16v8_merge_states(self.po, self.pl, self.seq_lens, self.chunk,
                                            self.out, self.lse)]
         side = torch.cuda.Stream(self.dev)
-        for fn in kinds:
+        for ki, fn in enumerate(kinds):
+            if ki == 0 and self.fused:
+                outs.append(0.0)
+                continue
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
                 for i in range(steps):
@@ -650,6 +669,19 @@ def main():
             "config": config_of(w8, label8, chunk8, b8.R)}}
     if not args.no_extra and args.workload == "1k":
         from fp8_paged_kv_append_gb300 import workloads
+        for name, (wf, _, cf) in (("decode_1k_b32", make_workload("1k")),
+                                  ("decode_8k_b16", make_workload("8k"))):
+            torch.cuda.empty_cache()
+            bf = DecodeBench(wf, device, split_chunk=cf, fused=True)
+            msf, segf = bf.run(max(10, args.steps // 2), 3)
+            sf = float(np.mean(segf[:, 1])) * 1e3
+            line["extra"][f"{name}_fused_append"] = {
+                "us_per_layer_step": round(msf * 1e3, 2),
+                "value": round(kv_bytes(wf) / (msf * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "kernel_us": {"decode_append_split": round(sf, 2),
+                              "merge_states": round(float(np.mean(segf[:, 2])) * 1e3, 2)},
+                "step": "append fused into the split kernel, then merge (2 launches)"}
+            del bf
         torch.cuda.empty_cache()
         line["extra"]["fullpool_40_layers"] = fullpool_line(device, 10, 3, hbm_peak)
         _, tpeak, tkind = load_peaks()

@@ -49,9 +49,13 @@ struct __align__(128) WarpRing {
   uint64_t bar[kStages];
 };
 
+__host__ __device__ constexpr size_t ids_bytes(int split_chunk) {
+  return ((static_cast<size_t>(split_chunk / kPage) * sizeof(int) + 15) / 16) * 16;
+}
+constexpr size_t kPatchBytes = kHeadDim * 2 + kHeadDim;  // new K row (fp16) + V row (E4M3)
+
 static size_t decode_smem_bytes(int split_chunk) {
-  const size_t ids = static_cast<size_t>(split_chunk / kPage) * sizeof(int);
-  return kWarps * sizeof(WarpRing) + ((ids + 15) / 16) * 16;
+  return kWarps * sizeof(WarpRing) + ids_bytes(split_chunk) + kPatchBytes;
 }
 
 // acc += a.lo * b.lo + a.hi * b.hi with fp16 operands, fp32 accumulation
@@ -90,16 +94,23 @@ __device__ __forceinline__ float reduce_scatter8(const float (&acc)[kGroup], int
   return kp;
 }
 
+// kAppend: also write each sequence's new token (k_new / v_new, position
+// L - 1) into the cache -- the CTA whose chunk holds that position does it
+// and patches the row into its shared-memory copy of the page, so the
+// attention sees the quantised value without a separate append launch.
+template <bool kAppend>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
-    const __half *__restrict__ q, const __half *__restrict__ k_cache,
-    const uint8_t *__restrict__ v_cache, const float *__restrict__ v_scale,
-    const int32_t *__restrict__ block_table, int32_t maxp, const int32_t *__restrict__ seq_lens,
-    int32_t hq, int32_t hkv, int32_t num_pages, float sm_scale, int32_t chunk,
-    int32_t max_chunks, float *__restrict__ part_o, float *__restrict__ part_lse,
-    int32_t *dev_error) {
+    const __half *__restrict__ q, __half *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+    const float *__restrict__ v_scale, const int32_t *__restrict__ block_table, int32_t maxp,
+    const int32_t *__restrict__ seq_lens, int32_t hq, int32_t hkv, int32_t num_pages,
+    float sm_scale, int32_t chunk, int32_t max_chunks, float *__restrict__ part_o,
+    float *__restrict__ part_lse, const __half *__restrict__ k_new,
+    const __half *__restrict__ v_new, int32_t *dev_error) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   WarpRing *rings = reinterpret_cast<WarpRing *>(smem_raw);
   int *page_ids = reinterpret_cast<int *>(smem_raw + kWarps * sizeof(WarpRing));
+  uint8_t *patch_k = smem_raw + kWarps * sizeof(WarpRing) + ids_bytes(chunk);
+  uint8_t *patch_v = patch_k + kHeadDim * 2;
 
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,6 +135,40 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
       pid = -1;
     }
     page_ids[i] = pid;
+  }
+  // Page (within this chunk) that receives the new token, or -1.
+  int patch_page = -1;
+  if constexpr (kAppend) {
+    if (L > 0 && (L - 1) / chunk == c) {
+      const int pos = L - 1;
+      patch_page = pos / kPage - start / kPage;
+      if (threadIdx.x < kHeadDim / 8) {
+        const int cc = threadIdx.x;  // 8 elements each
+        const int64_t src = (static_cast<int64_t>(b) * hkv + g) * kHeadDim + cc * 8;
+        const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+        const uint4 vraw = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+        const __half2 *vh = reinterpret_cast<const __half2 *>(&vraw);
+        const float sc = __ldg(v_scale + g);
+        uint32_t w[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float2 a = __half22float2(vh[2 * i]);
+          const float2 bb = __half22float2(vh[2 * i + 1]);
+          w[i] = static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc))) |
+                 (static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(bb.x, sc), __fdiv_rn(bb.y, sc)))
+                  << 16);
+        }
+        *reinterpret_cast<uint4 *>(patch_k + cc * 16) = kv;
+        *reinterpret_cast<uint2 *>(patch_v + cc * 8) = make_uint2(w[0], w[1]);
+        const int pid = __ldg(bt + patch_page);
+        if (pid >= 0 && pid < num_pages) {
+          const int64_t dst = ((static_cast<int64_t>(pid) * hkv + g) * kPage + pos % kPage) *
+                                  kHeadDim + cc * 8;
+          *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
+          *reinterpret_cast<uint2 *>(v_cache + dst) = make_uint2(w[0], w[1]);
+        }
+      }
+    }
   }
   WarpRing &ring = rings[warp];
   if (lane == 0) {
@@ -189,6 +234,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
     if (!ok) break;
     const int i = warp + k * kWarps;  // page within the chunk
     const int valid = min(kPage, n_tok - i * kPage);
+    if (kAppend && i == patch_page) {
+      // the copy may predate this kernel's write: put the new row in place
+      const int row = (L - 1) % kPage;
+      *reinterpret_cast<uint2 *>(ring.k[s] + row * 256 + lane * 8) =
+          *reinterpret_cast<const uint2 *>(patch_k + lane * 8);
+      *reinterpret_cast<uint32_t *>(ring.v[s] + row * kHeadDim + lane * 4) =
+          *reinterpret_cast<const uint32_t *>(patch_v + lane * 4);
+      __syncwarp();
+    }
     if (page_ids[i] >= 0) {
       // ---- scores of 16 tokens x 4 heads ----
       const uint8_t *kp = ring.k[s];
@@ -426,13 +480,15 @@ static bool ws_layout(int32_t batch, int32_t hq, int32_t d, int32_t max_seq_len,
   return true;
 }
 
+template <bool kAppend>
 static int32_t set_smem_attr(size_t bytes) {
   // The attribute is per device; remember the largest size configured.
   static size_t configured[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return K16V8_ERR_CUDA;
   if (dev < 64 && configured[dev] >= bytes) return K16V8_OK;
-  if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_split_kernel<kAppend>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(bytes)) != cudaSuccess)
     return K16V8_ERR_CUDA;
   if (dev < 64) configured[dev] = bytes;
@@ -472,12 +528,15 @@ extern "C" int32_t k16v8_decode_workspace_layout(int32_t batch, int32_t num_qo_h
   return K16V8_OK;
 }
 
-extern "C" int32_t k16v8_paged_decode_split(
-    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
-    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
-    int32_t max_seq_len, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
-    int32_t head_dim, int32_t num_pages, float sm_scale, int32_t split_chunk, void *workspace,
-    size_t workspace_bytes, int32_t *dev_error, void *stream) {
+template <bool kAppend>
+static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v_cache,
+                            const float *v_scale, const int32_t *block_table,
+                            int32_t max_pages_per_seq, const int32_t *seq_lens,
+                            int32_t max_seq_len, int32_t batch, int32_t num_qo_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t num_pages,
+                            float sm_scale, int32_t split_chunk, void *workspace,
+                            size_t workspace_bytes, const void *k_new, const void *v_new,
+                            int32_t *dev_error, void *stream) {
   int32_t st = check_attention_shape(num_qo_heads, num_kv_heads, head_dim);
   if (st != K16V8_OK) return st;
   if (batch < 0 || max_seq_len < 0 || num_pages <= 0 || max_pages_per_seq < 0)
@@ -492,6 +551,8 @@ extern "C" int32_t k16v8_paged_decode_split(
   if (batch == 0) return K16V8_OK;
   if (!q || !k_cache || !v_cache || !v_scale || !block_table || !seq_lens || !workspace)
     return K16V8_ERR_INVALID_ARG;
+  if (kAppend && (!k_new || !v_new || !k16v8_aligned(k_new, 16) || !k16v8_aligned(v_new, 16)))
+    return K16V8_ERR_INVALID_ARG;
   if (workspace_bytes < w.total) return K16V8_ERR_WORKSPACE_TOO_SMALL;
   if (!k16v8_aligned(q, 16) || !k16v8_aligned(k_cache, 16) || !k16v8_aligned(v_cache, 16) ||
       !k16v8_aligned(workspace, 256) || !k16v8_aligned(block_table, 4) ||
@@ -499,16 +560,43 @@ extern "C" int32_t k16v8_paged_decode_split(
     return K16V8_ERR_INVALID_ARG;
   if (max_seq_len == 0) return K16V8_OK;  // every sequence empty: nothing to read
   const size_t smem = decode_smem_bytes(split_chunk);
-  st = set_smem_attr(smem);
+  st = set_smem_attr<kAppend>(smem);
   if (st != K16V8_OK) return st;
   float *po = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_off);
   float *pl = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.lse_off);
   const dim3 grid(w.chunks, num_kv_heads, batch);
-  return k16v8_launch_pdl(decode_split_kernel, grid, dim3(kWarps * 32), smem,
-                          static_cast<cudaStream_t>(stream), static_cast<const __half *>(q),
-                          static_cast<const __half *>(k_cache), v_cache, v_scale, block_table,
-                          max_pages_per_seq, seq_lens, num_qo_heads, num_kv_heads, num_pages,
-                          sm_scale, split_chunk, w.chunks, po, pl, dev_error);
+  return k16v8_launch_pdl(
+      decode_split_kernel<kAppend>, grid, dim3(kWarps * 32), smem,
+      static_cast<cudaStream_t>(stream), static_cast<const __half *>(q),
+      static_cast<__half *>(const_cast<void *>(k_cache)), const_cast<uint8_t *>(v_cache), v_scale,
+      block_table, max_pages_per_seq, seq_lens, num_qo_heads, num_kv_heads, num_pages, sm_scale,
+      split_chunk, w.chunks, po, pl, static_cast<const __half *>(k_new),
+      static_cast<const __half *>(v_new), dev_error);
+}
+
+extern "C" int32_t k16v8_paged_decode_split(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t max_seq_len, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, int32_t split_chunk, void *workspace,
+    size_t workspace_bytes, int32_t *dev_error, void *stream) {
+  return launch_split<false>(q, k_cache, v_cache, v_scale, block_table, max_pages_per_seq,
+                             seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim,
+                             num_pages, sm_scale, split_chunk, workspace, workspace_bytes, nullptr,
+                             nullptr, dev_error, stream);
+}
+
+extern "C" int32_t k16v8_paged_decode_append_split(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, uint8_t *v_cache,
+    const float *v_scale, const int32_t *block_table, int32_t max_pages_per_seq,
+    const int32_t *seq_lens, int32_t max_seq_len, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale,
+    int32_t split_chunk, void *workspace, size_t workspace_bytes, int32_t *dev_error,
+    void *stream) {
+  return launch_split<true>(q, k_cache, v_cache, v_scale, block_table, max_pages_per_seq,
+                            seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim,
+                            num_pages, sm_scale, split_chunk, workspace, workspace_bytes, k_new,
+                            v_new, dev_error, stream);
 }
 
 extern "C" int32_t k16v8_merge_states(const float *partial_o, const float *partial_lse,
@@ -544,6 +632,28 @@ extern "C" int32_t k16v8_paged_decode_attention(
                                         max_pages_per_seq, seq_lens, max_seq_len, batch,
                                         num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale,
                                         split_chunk, workspace, workspace_bytes, dev_error, stream);
+  if (st != K16V8_OK || batch == 0) return st;
+  WsLayout w;
+  ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w);
+  const uint8_t *base = static_cast<const uint8_t *>(workspace);
+  return k16v8_merge_states(reinterpret_cast<const float *>(base + w.o_off),
+                            reinterpret_cast<const float *>(base + w.lse_off), batch,
+                            num_qo_heads, w.chunks, head_dim, seq_lens, split_chunk, out, lse,
+                            stream);
+}
+
+extern "C" int32_t k16v8_paged_decode_append_attention(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, uint8_t *v_cache,
+    const float *v_scale, const int32_t *block_table, int32_t max_pages_per_seq,
+    const int32_t *seq_lens, int32_t max_seq_len, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale,
+    int32_t split_chunk, void *workspace, size_t workspace_bytes, void *out, float *lse,
+    int32_t *dev_error, void *stream) {
+  if (batch > 0 && !out) return K16V8_ERR_INVALID_ARG;
+  int32_t st = k16v8_paged_decode_append_split(
+      q, k_new, v_new, k_cache, v_cache, v_scale, block_table, max_pages_per_seq, seq_lens,
+      max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale, split_chunk,
+      workspace, workspace_bytes, dev_error, stream);
   if (st != K16V8_OK || batch == 0) return st;
   WsLayout w;
   ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w);

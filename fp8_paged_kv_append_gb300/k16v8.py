@@ -49,6 +49,12 @@ SIGNATURES = {
     "k16v8_paged_decode_attention_static": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32,
                                                    _i32, _i32, _i32, _i32, _f32, _i32, _P, _P,
                                                    _P, _P]),
+    "k16v8_paged_decode_append_split": (_i32, [_P, _P, _P, _P, _P, _P, _P, _i32, _P, _i32, _i32,
+                                               _i32, _i32, _i32, _i32, _f32, _i32, _P, _sz, _P,
+                                               _P]),
+    "k16v8_paged_decode_append_attention": (_i32, [_P, _P, _P, _P, _P, _P, _P, _i32, _P, _i32,
+                                                   _i32, _i32, _i32, _i32, _i32, _f32, _i32, _P,
+                                                   _sz, _P, _P, _P, _P]),
     "k16v8_paged_prefill_attention": (_i32, [_P, _P, _i32, _i32, _P, _P, _P, _P, _i32, _P,
                                              _i32, _i32, _i32, _i32, _i32, _f32, _P, _P, _P,
                                              _P]),
@@ -184,6 +190,34 @@ def k16v8_paged_decode_attention(q, k_cache, v_cache, v_scale, block_table, seq_
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _ptr(dev_error),
         _stream(stream))
     _check("k16v8_paged_decode_attention", st)
+
+
+def k16v8_paged_decode_append_split(q, k_new, v_new, k_cache, v_cache, v_scale, block_table,
+                                    seq_lens, max_seq_len, sm_scale, split_chunk, workspace,
+                                    dev_error=None, stream=None):
+    """Decode split with each sequence's new token (k_new / v_new fp16
+    [B, Hkv, D]) written at position seq_lens[b] - 1 by the same kernel."""
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_append_split(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale),
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_seq_len), B, hq,
+        k_cache.shape[1], d, k_cache.shape[0], float(sm_scale), int(split_chunk),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_error),
+        _stream(stream))
+    _check("k16v8_paged_decode_append_split", st)
+
+
+def k16v8_paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, v_scale, block_table,
+                                        seq_lens, max_seq_len, sm_scale, split_chunk, workspace,
+                                        out, lse=None, dev_error=None, stream=None):
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_append_attention(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale),
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_seq_len), B, hq,
+        k_cache.shape[1], d, k_cache.shape[0], float(sm_scale), int(split_chunk),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+        _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_decode_append_attention", st)
 
 
 def k16v8_paged_prefill_attention(q, qo_indptr, max_qlen, k_cache, v_cache, v_scale,

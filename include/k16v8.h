@@ -191,6 +191,40 @@ int32_t k16v8_paged_decode_attention(const void *q, const void *k_cache,
                                      int32_t *dev_error, void *stream);
 
 /*
+ * paged_decode_append_split / paged_decode_append_attention -- one decode
+ * step's cache write fused into the attention kernel: equivalent to
+ * k16v8_kv_append of each sequence's new token at position seq_lens[b] - 1
+ * (slot block_table[b][(L-1)/16]*16 + (L-1)%16) followed by
+ * k16v8_paged_decode_split (and, for _attention, k16v8_merge_states), in one
+ * kernel instead of two.  "The candidate also gathers values and writes the
+ * compressed cache" ("Matched diagnostic profiles") is the step folded in.
+ *
+ *   k_new, v_new  device fp16 [batch][num_kv_heads][head_dim], contiguous,
+ *                 16-B aligned: the K and V of each sequence's new token
+ *   seq_lens      lengths INCLUDING the new token (a sequence with L = 0 has
+ *                 no new token and is skipped)
+ * Other arguments as for k16v8_paged_decode_split / _attention.  The cache
+ * row is written with the same rounding as k16v8_kv_append.
+ */
+int32_t k16v8_paged_decode_append_split(const void *q, const void *k_new, const void *v_new,
+                                        void *k_cache, uint8_t *v_cache, const float *v_scale,
+                                        const int32_t *block_table, int32_t max_pages_per_seq,
+                                        const int32_t *seq_lens, int32_t max_seq_len,
+                                        int32_t batch, int32_t num_qo_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t num_pages, float sm_scale, int32_t split_chunk,
+                                        void *workspace, size_t workspace_bytes,
+                                        int32_t *dev_error, void *stream);
+
+int32_t k16v8_paged_decode_append_attention(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, uint8_t *v_cache,
+    const float *v_scale, const int32_t *block_table, int32_t max_pages_per_seq,
+    const int32_t *seq_lens, int32_t max_seq_len, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale,
+    int32_t split_chunk, void *workspace, size_t workspace_bytes, void *out, float *lse,
+    int32_t *dev_error, void *stream);
+
+/*
  * paged_prefill_attention -- causal attention of a chunk of new prompt tokens
  * against the paged cache, on tensor cores.  The page's throughput metric
  * includes prefill ("Fixed throughput studies"); its 8K profile admits fresh
