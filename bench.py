@@ -355,6 +355,71 @@ class DecodeBench:
         return dt, h2d, d2h
 
 
+# ---- the FP16-KV control on the same kernels ---------------------------------------
+
+def fp16_control_line(w, device, chunk, steps, warmup, hbm_peak):
+    """Decode step (append + split + merge) over a pool whose values are fp16
+    (5,120 B per token per layer), same workload and launch shape."""
+    import torch
+    from fp8_paged_kv_append_gb300 import k16v8 as K
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    B, hq, d = w.q.shape
+    P = w.num_pages
+    R = max(1, -(-4 * L2_BYTES // (P * w.num_kv_heads * 16 * d * 4)))
+    kc = torch.empty((R * P, w.num_kv_heads, 16, d), dtype=torch.float16, device=device)
+    vc = torch.empty_like(kc)
+    k_all, v_all = td(w.k_tok), td(w.v_tok.astype(np.float16))
+    bts, slots = [], []
+    for r in range(R):
+        K.k16v8_kv_append_v16(k_all, v_all, td(w.slot_mapping + r * P * 16), kc, vc)
+        bts.append(td(w.block_table + r * P))
+        slots.append(td(w.slot_mapping[w.new_rows] + r * P * 16))
+    del k_all, v_all
+    k_new, v_new = td(w.k_tok[w.new_rows]), td(w.v_tok[w.new_rows].astype(np.float16))
+    q, lens = td(w.q), td(w.seq_lens)
+    L = int(w.seq_lens.max())
+    ws = torch.empty(K.k16v8_decode_workspace_size(B, hq, d, L, chunk), dtype=torch.uint8,
+                     device=device)
+    po, pl = K.workspace_views(ws, B, hq, d, L, chunk)
+    out = torch.empty((B, hq, d), dtype=torch.float16, device=device)
+    lse = torch.empty((B, hq), dtype=torch.float32, device=device)
+
+    def split(i):
+        K.k16v8_paged_decode_split_v16(q, kc, vc, bts[i % R], lens, L, w.sm_scale, chunk, ws)
+
+    def step(i):
+        K.k16v8_kv_append_v16(k_new, v_new, slots[i % R], kc, vc)
+        split(i)
+        K.k16v8_merge_states(po, pl, lens, chunk, out, lse)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    side = torch.cuda.Stream(device)
+    times = []
+    for fn in (step, split):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+            for i in range(steps):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize(device)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        g.replay()
+        t1.record()
+        torch.cuda.synchronize(device)
+        times.append(t0.elapsed_time(t1) / steps)
+    kvb = int(w.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * d * 4
+    split_bytes = kvb + B * hq * d * 2
+    return {"us_per_layer_step": round(times[0] * 1e3, 2),
+            "split_us": round(times[1] * 1e3, 2),
+            "kv_bytes_per_step": kvb, "value": round(kvb / (times[0] * 1e-3) / 1e9, 1),
+            "unit": "GB/s",
+            "split_frac_of_hbm_peak": round(split_bytes / (times[1] * 1e-3) / 1e9 / hbm_peak, 4)}
+
+
 # ---- chunked prefill on the GPU --------------------------------------------------
 
 def prefill_flops(p) -> float:
@@ -682,6 +747,14 @@ def main():
                               "merge_states": round(float(np.mean(segf[:, 2])) * 1e3, 2)},
                 "step": "append fused into the split kernel, then merge (2 launches)"}
             del bf
+        for name, (wf, _, cf) in (("decode_1k_b32", make_workload("1k")),
+                                  ("decode_8k_b16", make_workload("8k"))):
+            torch.cuda.empty_cache()
+            ctl = fp16_control_line(wf, device, cf, max(10, args.steps // 2), 3, hbm_peak)
+            k16 = line["us_per_layer_step"] if name == "decode_1k_b32" else \
+                line["extra"]["decode_8k_b16"]["us_per_layer_step"]
+            ctl["k16v8_speedup_over_fp16_kv"] = round(ctl["us_per_layer_step"] / k16, 3)
+            line["extra"][f"{name}_fp16_kv_control"] = ctl
         torch.cuda.empty_cache()
         line["extra"]["fullpool_40_layers"] = fullpool_line(device, 10, 3, hbm_peak)
         _, tpeak, tkind = load_peaks()

@@ -41,21 +41,22 @@ constexpr int kKPageBytes = kPage * kHeadDim * 2;  // 4096
 constexpr int kVPageBytes = kPage * kHeadDim;      // 2048
 constexpr unsigned kFull = 0xffffffffu;
 
-struct __align__(128) WarpRing {
+template <int kVBytes>
+struct __align__(128) WarpRingT {
   uint8_t k[kStages][kKPageBytes];
-  uint8_t v[kStages][kVPageBytes];
+  uint8_t v[kStages][kVBytes];
   uint32_t p[kPage * kGroup];  // p[token][head] as a duplicated fp16 pair (p, p)
   float alpha[kGroup];         // rescale factor of the running state
   uint64_t bar[kStages];
 };
+using WarpRing = WarpRingT<kVPageBytes>;             // E4M3 values
+using WarpRing16 = WarpRingT<2 * kVPageBytes>;       // FP16 values (the FP16-KV control)
 
 __host__ __device__ constexpr size_t ids_bytes(int split_chunk) {
   return ((static_cast<size_t>(split_chunk / kPage) * sizeof(int) + 15) / 16) * 16;
 }
-constexpr size_t kPatchBytes = kHeadDim * 2 + kHeadDim;  // new K row (fp16) + V row (E4M3)
-
-static size_t decode_smem_bytes(int split_chunk) {
-  return kWarps * sizeof(WarpRing) + ids_bytes(split_chunk) + kPatchBytes;
+static size_t decode_smem_bytes(int split_chunk, bool vf16) {
+  return kWarps * (vf16 ? sizeof(WarpRing16) : sizeof(WarpRing)) + ids_bytes(split_chunk);
 }
 
 // acc += a.lo * b.lo + a.hi * b.hi with fp16 operands, fp32 accumulation
@@ -95,22 +96,24 @@ __device__ __forceinline__ float reduce_scatter8(const float (&acc)[kGroup], int
 }
 
 // kAppend: also write each sequence's new token (k_new / v_new, position
-// L - 1) into the cache -- the CTA whose chunk holds that position does it
-// and patches the row into its shared-memory copy of the page, so the
+// L - 1) into the cache -- the warp that consumes that page quantises the
+// row, stores it, and writes it into its staged copy of the page, so the
 // attention sees the quantised value without a separate append launch.
-template <bool kAppend>
-__global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
+// kVF16: the FP16-KV control -- values stored as fp16 (4 KB per page
+// tile), no dequantisation and no scale.
+template <bool kAppend, bool kVF16>
+__global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_split_kernel(
     const __half *__restrict__ q, __half *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
     const float *__restrict__ v_scale, const int32_t *__restrict__ block_table, int32_t maxp,
     const int32_t *__restrict__ seq_lens, int32_t hq, int32_t hkv, int32_t num_pages,
     float sm_scale, int32_t chunk, int32_t max_chunks, float *__restrict__ part_o,
     float *__restrict__ part_lse, const __half *__restrict__ k_new,
     const __half *__restrict__ v_new, int32_t *dev_error) {
+  using Ring = WarpRingT<kVF16 ? 2 * kVPageBytes : kVPageBytes>;
+  constexpr uint32_t kVTile = kVF16 ? 2 * kVPageBytes : kVPageBytes;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  WarpRing *rings = reinterpret_cast<WarpRing *>(smem_raw);
-  int *page_ids = reinterpret_cast<int *>(smem_raw + kWarps * sizeof(WarpRing));
-  uint8_t *patch_k = smem_raw + kWarps * sizeof(WarpRing) + ids_bytes(chunk);
-  uint8_t *patch_v = patch_k + kHeadDim * 2;
+  Ring *rings = reinterpret_cast<Ring *>(smem_raw);
+  int *page_ids = reinterpret_cast<int *>(smem_raw + kWarps * sizeof(Ring));
 
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,38 +142,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
   // Page (within this chunk) that receives the new token, or -1.
   int patch_page = -1;
   if constexpr (kAppend) {
-    if (L > 0 && (L - 1) / chunk == c) {
-      const int pos = L - 1;
-      patch_page = pos / kPage - start / kPage;
-      if (threadIdx.x < kHeadDim / 8) {
-        const int cc = threadIdx.x;  // 8 elements each
-        const int64_t src = (static_cast<int64_t>(b) * hkv + g) * kHeadDim + cc * 8;
-        const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
-        const uint4 vraw = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
-        const __half2 *vh = reinterpret_cast<const __half2 *>(&vraw);
-        const float sc = __ldg(v_scale + g);
-        uint32_t w[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float2 a = __half22float2(vh[2 * i]);
-          const float2 bb = __half22float2(vh[2 * i + 1]);
-          w[i] = static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc))) |
-                 (static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(bb.x, sc), __fdiv_rn(bb.y, sc)))
-                  << 16);
-        }
-        *reinterpret_cast<uint4 *>(patch_k + cc * 16) = kv;
-        *reinterpret_cast<uint2 *>(patch_v + cc * 8) = make_uint2(w[0], w[1]);
-        const int pid = __ldg(bt + patch_page);
-        if (pid >= 0 && pid < num_pages) {
-          const int64_t dst = ((static_cast<int64_t>(pid) * hkv + g) * kPage + pos % kPage) *
-                                  kHeadDim + cc * 8;
-          *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
-          *reinterpret_cast<uint2 *>(v_cache + dst) = make_uint2(w[0], w[1]);
-        }
-      }
-    }
+    if (L > 0 && (L - 1) / chunk == c) patch_page = (L - 1) / kPage - start / kPage;
   }
-  WarpRing &ring = rings[warp];
+  Ring &ring = rings[warp];
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) mbar_init(&ring.bar[s], 1);
@@ -189,9 +163,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
       return;
     }
     const int64_t tile = (static_cast<int64_t>(pid) * hkv + g) * head_tile;
-    mbar_arrive_expect_tx(&ring.bar[s], kKPageBytes + kVPageBytes);
+    mbar_arrive_expect_tx(&ring.bar[s], kKPageBytes + kVTile);
     bulk_g2s_evict_first(ring.k[s], k_cache + tile, kKPageBytes, &ring.bar[s], policy);
-    bulk_g2s_evict_first(ring.v[s], v_cache + tile, kVPageBytes, &ring.bar[s], policy);
+    bulk_g2s_evict_first(ring.v[s], v_cache + tile * (kVF16 ? 2 : 1), kVTile, &ring.bar[s],
+                         policy);
   };
   if (lane == 0)
     for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
@@ -235,12 +210,34 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
     const int i = warp + k * kWarps;  // page within the chunk
     const int valid = min(kPage, n_tok - i * kPage);
     if (kAppend && i == patch_page) {
-      // the copy may predate this kernel's write: put the new row in place
-      const int row = (L - 1) % kPage;
-      *reinterpret_cast<uint2 *>(ring.k[s] + row * 256 + lane * 8) =
-          *reinterpret_cast<const uint2 *>(patch_k + lane * 8);
-      *reinterpret_cast<uint32_t *>(ring.v[s] + row * kHeadDim + lane * 4) =
-          *reinterpret_cast<const uint32_t *>(patch_v + lane * 4);
+      // Quantise the new token, store it in the cache, and put the same row
+      // into the staged copy of the page (the copy may predate the store).
+      if (lane < kHeadDim / 8) {
+        const int row = (L - 1) % kPage;
+        const int64_t src = (static_cast<int64_t>(b) * hkv + g) * kHeadDim + lane * 8;
+        const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+        const uint4 vraw = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+        const __half2 *vh = reinterpret_cast<const __half2 *>(&vraw);
+        const float sc = __ldg(v_scale + g);
+        uint32_t w[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float2 a = __half22float2(vh[2 * u]);
+          const float2 bb = __half22float2(vh[2 * u + 1]);
+          w[u] = static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc))) |
+                 (static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(bb.x, sc), __fdiv_rn(bb.y, sc)))
+                  << 16);
+        }
+        *reinterpret_cast<uint4 *>(ring.k[s] + row * 256 + lane * 16) = kv;
+        *reinterpret_cast<uint2 *>(ring.v[s] + row * kHeadDim + lane * 8) = make_uint2(w[0], w[1]);
+        const int pid = page_ids[i];
+        if (pid >= 0) {
+          const int64_t dst =
+              ((static_cast<int64_t>(pid) * hkv + g) * kPage + row) * kHeadDim + lane * 8;
+          *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
+          *reinterpret_cast<uint2 *>(v_cache + dst) = make_uint2(w[0], w[1]);
+        }
+      }
       __syncwarp();
     }
     if (page_ids[i] >= 0) {
@@ -292,12 +289,19 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
       __half2 acc[kGroup][2];
 #pragma unroll
       for (int h = 0; h < kGroup; ++h) acc[h][0] = acc[h][1] = __float2half2_rn(0.f);
-      const uint8_t *vp = ring.v[s] + lane * 4;
+      const uint8_t *vp = ring.v[s] + lane * (kVF16 ? 8 : 4);
       auto pv_token = [&](int t) {
-        const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp + t * kHeadDim);
+        __half2 v01, v23;
+        if constexpr (kVF16) {
+          const uint2 raw = *reinterpret_cast<const uint2 *>(vp + t * kHeadDim * 2);
+          v01 = *reinterpret_cast<const __half2 *>(&raw.x);
+          v23 = *reinterpret_cast<const __half2 *>(&raw.y);
+        } else {
+          const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp + t * kHeadDim);
+          v01 = e4m3x2_to_half2(static_cast<uint16_t>(raw & 0xffffu));
+          v23 = e4m3x2_to_half2(static_cast<uint16_t>(raw >> 16));
+        }
         const uint4 pp = *reinterpret_cast<const uint4 *>(ring.p + t * kGroup);
-        const __half2 v01 = e4m3x2_to_half2(static_cast<uint16_t>(raw & 0xffffu));
-        const __half2 v23 = e4m3x2_to_half2(static_cast<uint16_t>(raw >> 16));
         const uint32_t pw[kGroup] = {pp.x, pp.y, pp.z, pp.w};
 #pragma unroll
         for (int h = 0; h < kGroup; ++h) {
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) decode_split_kernel(
     float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
     float lse = -INFINITY;
     if (Ls > 0.f) {
-      const float inv = __ldg(v_scale + g) / Ls;
+      const float inv = (kVF16 ? 1.f : __ldg(v_scale + g)) / Ls;
       res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       lse = (M + lg2(Ls)) * kLn2;
     }
@@ -480,14 +484,14 @@ static bool ws_layout(int32_t batch, int32_t hq, int32_t d, int32_t max_seq_len,
   return true;
 }
 
-template <bool kAppend>
+template <bool kAppend, bool kVF16>
 static int32_t set_smem_attr(size_t bytes) {
   // The attribute is per device; remember the largest size configured.
   static size_t configured[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return K16V8_ERR_CUDA;
   if (dev < 64 && configured[dev] >= bytes) return K16V8_OK;
-  if (cudaFuncSetAttribute(decode_split_kernel<kAppend>,
+  if (cudaFuncSetAttribute(decode_split_kernel<kAppend, kVF16>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(bytes)) != cudaSuccess)
     return K16V8_ERR_CUDA;
@@ -528,7 +532,7 @@ extern "C" int32_t k16v8_decode_workspace_layout(int32_t batch, int32_t num_qo_h
   return K16V8_OK;
 }
 
-template <bool kAppend>
+template <bool kAppend, bool kVF16 = false>
 static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v_cache,
                             const float *v_scale, const int32_t *block_table,
                             int32_t max_pages_per_seq, const int32_t *seq_lens,
@@ -549,7 +553,8 @@ static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v
   if (!ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w))
     return K16V8_ERR_INVALID_ARG;
   if (batch == 0) return K16V8_OK;
-  if (!q || !k_cache || !v_cache || !v_scale || !block_table || !seq_lens || !workspace)
+  if (!q || !k_cache || !v_cache || (!kVF16 && !v_scale) || !block_table || !seq_lens ||
+      !workspace)
     return K16V8_ERR_INVALID_ARG;
   if (kAppend && (!k_new || !v_new || !k16v8_aligned(k_new, 16) || !k16v8_aligned(v_new, 16)))
     return K16V8_ERR_INVALID_ARG;
@@ -559,14 +564,14 @@ static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v
       !k16v8_aligned(seq_lens, 4) || !k16v8_aligned(v_scale, 4))
     return K16V8_ERR_INVALID_ARG;
   if (max_seq_len == 0) return K16V8_OK;  // every sequence empty: nothing to read
-  const size_t smem = decode_smem_bytes(split_chunk);
-  st = set_smem_attr<kAppend>(smem);
+  const size_t smem = decode_smem_bytes(split_chunk, kVF16);
+  st = set_smem_attr<kAppend, kVF16>(smem);
   if (st != K16V8_OK) return st;
   float *po = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_off);
   float *pl = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.lse_off);
   const dim3 grid(w.chunks, num_kv_heads, batch);
   return k16v8_launch_pdl(
-      decode_split_kernel<kAppend>, grid, dim3(kWarps * 32), smem,
+      decode_split_kernel<kAppend, kVF16>, grid, dim3(kWarps * 32), smem,
       static_cast<cudaStream_t>(stream), static_cast<const __half *>(q),
       static_cast<__half *>(const_cast<void *>(k_cache)), const_cast<uint8_t *>(v_cache), v_scale,
       block_table, max_pages_per_seq, seq_lens, num_qo_heads, num_kv_heads, num_pages, sm_scale,
@@ -597,6 +602,19 @@ extern "C" int32_t k16v8_paged_decode_append_split(
                             seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim,
                             num_pages, sm_scale, split_chunk, workspace, workspace_bytes, k_new,
                             v_new, dev_error, stream);
+}
+
+extern "C" int32_t k16v8_paged_decode_split_v16(
+    const void *q, const void *k_cache, const void *v_cache16, const int32_t *block_table,
+    int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_pages,
+    float sm_scale, int32_t split_chunk, void *workspace, size_t workspace_bytes,
+    int32_t *dev_error, void *stream) {
+  return launch_split<false, true>(
+      q, k_cache, static_cast<const uint8_t *>(v_cache16), nullptr, block_table,
+      max_pages_per_seq, seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim,
+      num_pages, sm_scale, split_chunk, workspace, workspace_bytes, nullptr, nullptr, dev_error,
+      stream);
 }
 
 extern "C" int32_t k16v8_merge_states(const float *partial_o, const float *partial_lse,
@@ -654,6 +672,28 @@ extern "C" int32_t k16v8_paged_decode_append_attention(
       q, k_new, v_new, k_cache, v_cache, v_scale, block_table, max_pages_per_seq, seq_lens,
       max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale, split_chunk,
       workspace, workspace_bytes, dev_error, stream);
+  if (st != K16V8_OK || batch == 0) return st;
+  WsLayout w;
+  ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w);
+  const uint8_t *base = static_cast<const uint8_t *>(workspace);
+  return k16v8_merge_states(reinterpret_cast<const float *>(base + w.o_off),
+                            reinterpret_cast<const float *>(base + w.lse_off), batch,
+                            num_qo_heads, w.chunks, head_dim, seq_lens, split_chunk, out, lse,
+                            stream);
+}
+
+extern "C" int32_t k16v8_paged_decode_attention_v16(
+    const void *q, const void *k_cache, const void *v_cache16, const int32_t *block_table,
+    int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_pages,
+    float sm_scale, int32_t split_chunk, void *workspace, size_t workspace_bytes, void *out,
+    float *lse, int32_t *dev_error, void *stream) {
+  if (batch > 0 && !out) return K16V8_ERR_INVALID_ARG;
+  int32_t st = k16v8_paged_decode_split_v16(q, k_cache, v_cache16, block_table,
+                                            max_pages_per_seq, seq_lens, max_seq_len, batch,
+                                            num_qo_heads, num_kv_heads, head_dim, num_pages,
+                                            sm_scale, split_chunk, workspace, workspace_bytes,
+                                            dev_error, stream);
   if (st != K16V8_OK || batch == 0) return st;
   WsLayout w;
   ws_layout(batch, num_qo_heads, head_dim, max_seq_len, split_chunk, &w);

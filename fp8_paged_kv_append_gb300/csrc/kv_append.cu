@@ -14,7 +14,9 @@
 
 namespace k16v8 {
 
-template <bool kVF32>
+// kVF32: fp32 input values.  kV16: the FP16-KV control -- values are copied
+// as fp16 into a 2-byte value cache (no scale, no quantisation).
+template <bool kVF32, bool kV16 = false>
 __global__ void __launch_bounds__(256) kv_append_kernel(
     const __half *__restrict__ k, int64_t k_ts, const void *__restrict__ v, int64_t v_ts,
     const int64_t *__restrict__ slot_mapping, int32_t num_tokens,
@@ -45,6 +47,13 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k + t * k_ts + h * kHeadDim + c * 8));
     *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
 
+    if constexpr (kV16) {
+      const uint4 raw = __ldg(
+          reinterpret_cast<const uint4 *>(static_cast<const __half *>(v) + t * v_ts +
+                                          h * kHeadDim + c * 8));
+      *reinterpret_cast<uint4 *>(reinterpret_cast<__half *>(v_cache) + dst) = raw;
+      continue;
+    }
     // V: widen to fp32, IEEE divide by the head's scale, round to E4M3.
     float x[8];
     const int64_t vsrc = t * v_ts + h * kHeadDim + c * 8;
@@ -122,4 +131,34 @@ extern "C" int32_t k16v8_kv_append(const void *k, int64_t k_token_stride, const 
                           static_cast<const __half *>(k), k_token_stride, v, v_token_stride,
                           slot_mapping, num_tokens, v_scale, static_cast<__half *>(k_cache),
                           v_cache, num_pages, num_kv_heads, dev_error);
+}
+
+extern "C" int32_t k16v8_kv_append_v16(const void *k, int64_t k_token_stride, const void *v,
+                                       int64_t v_token_stride, const int64_t *slot_mapping,
+                                       int32_t num_tokens, void *k_cache, void *v_cache16,
+                                       int32_t num_pages, int32_t num_kv_heads, int32_t head_dim,
+                                       int32_t *dev_error, void *stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_pages <= 0) return K16V8_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return K16V8_ERR_UNSUPPORTED_SHAPE;
+  if (num_tokens == 0) return K16V8_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache16) return K16V8_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_token_stride == 0) k_token_stride = row;
+  if (v_token_stride == 0) v_token_stride = row;
+  if (k_token_stride < row || v_token_stride < row || k_token_stride % 8 || v_token_stride % 8)
+    return K16V8_ERR_INVALID_ARG;
+  if (!k16v8_aligned(k, 16) || !k16v8_aligned(v, 16) || !k16v8_aligned(k_cache, 16) ||
+      !k16v8_aligned(v_cache16, 16) || !k16v8_aligned(slot_mapping, 8))
+    return K16V8_ERR_INVALID_ARG;
+  const int sms = k16v8_sm_count();
+  if (sms <= 0) return K16V8_ERR_CUDA;
+  const int64_t units = static_cast<int64_t>(num_tokens) * num_kv_heads * (kHeadDim / 8);
+  int64_t blocks = (units + 255) / 256;
+  if (blocks > static_cast<int64_t>(sms) * 8) blocks = static_cast<int64_t>(sms) * 8;
+  return k16v8_launch_pdl(kv_append_kernel<false, true>, dim3(static_cast<unsigned>(blocks)),
+                          dim3(256), 0, static_cast<cudaStream_t>(stream),
+                          static_cast<const __half *>(k), k_token_stride, v, v_token_stride,
+                          slot_mapping, num_tokens, static_cast<const float *>(nullptr),
+                          static_cast<__half *>(k_cache), static_cast<uint8_t *>(v_cache16),
+                          num_pages, num_kv_heads, dev_error);
 }

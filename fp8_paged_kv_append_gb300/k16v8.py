@@ -55,6 +55,13 @@ SIGNATURES = {
     "k16v8_paged_decode_append_attention": (_i32, [_P, _P, _P, _P, _P, _P, _P, _i32, _P, _i32,
                                                    _i32, _i32, _i32, _i32, _i32, _f32, _i32, _P,
                                                    _sz, _P, _P, _P, _P]),
+    "k16v8_kv_append_v16": (_i32, [_P, _i64, _P, _i64, _P, _i32, _P, _P, _i32, _i32, _i32, _P,
+                                   _P]),
+    "k16v8_paged_decode_split_v16": (_i32, [_P, _P, _P, _P, _i32, _P, _i32, _i32, _i32, _i32,
+                                            _i32, _i32, _f32, _i32, _P, _sz, _P, _P]),
+    "k16v8_paged_decode_attention_v16": (_i32, [_P, _P, _P, _P, _i32, _P, _i32, _i32, _i32,
+                                                _i32, _i32, _i32, _f32, _i32, _P, _sz, _P, _P,
+                                                _P, _P]),
     "k16v8_paged_prefill_attention": (_i32, [_P, _P, _i32, _i32, _P, _P, _P, _P, _i32, _P,
                                              _i32, _i32, _i32, _i32, _i32, _f32, _P, _P, _P,
                                              _P]),
@@ -218,6 +225,40 @@ def k16v8_paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, v_sca
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
         _ptr(dev_error), _stream(stream))
     _check("k16v8_paged_decode_append_attention", st)
+
+
+def k16v8_kv_append_v16(k, v, slot_mapping, k_cache, v_cache16, dev_error=None, stream=None):
+    """FP16-KV control cache write (values copied as fp16)."""
+    T, hkv, d = k.shape
+    st = load_library().k16v8_kv_append_v16(
+        _ptr(k), _row_stride(k, "k"), _ptr(v), _row_stride(v, "v"), _ptr(slot_mapping), T,
+        _ptr(k_cache), _ptr(v_cache16), k_cache.shape[0], hkv, d, _ptr(dev_error),
+        _stream(stream))
+    _check("k16v8_kv_append_v16", st)
+
+
+def k16v8_paged_decode_split_v16(q, k_cache, v_cache16, block_table, seq_lens, max_seq_len,
+                                 sm_scale, split_chunk, workspace, dev_error=None, stream=None):
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_split_v16(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache16), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), int(max_seq_len), B, hq, k_cache.shape[1], d, k_cache.shape[0],
+        float(sm_scale), int(split_chunk), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_decode_split_v16", st)
+
+
+def k16v8_paged_decode_attention_v16(q, k_cache, v_cache16, block_table, seq_lens, max_seq_len,
+                                     sm_scale, split_chunk, workspace, out, lse=None,
+                                     dev_error=None, stream=None):
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_attention_v16(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache16), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), int(max_seq_len), B, hq, k_cache.shape[1], d, k_cache.shape[0],
+        float(sm_scale), int(split_chunk), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _ptr(dev_error),
+        _stream(stream))
+    _check("k16v8_paged_decode_attention_v16", st)
 
 
 def k16v8_paged_prefill_attention(q, qo_indptr, max_qlen, k_cache, v_cache, v_scale,

@@ -225,6 +225,42 @@ int32_t k16v8_paged_decode_append_attention(
     int32_t *dev_error, void *stream);
 
 /*
+ * FP16-KV control: the same cache write and split-KV decode for a pool that
+ * stores values as fp16 ([num_pages][num_kv_heads][16][head_dim], 2 bytes,
+ * no scale) -- the native controls of the subject page store FP16 keys and
+ * values (intro), 5,120 B per token per layer instead of 3,840.  Kept to
+ * measure the asymmetric format against it on the same kernels.
+ *   k16v8_kv_append_v16: k, v fp16 [num_tokens][num_kv_heads][head_dim]
+ *     (token strides as for k16v8_kv_append) copied to the caches.
+ *   k16v8_paged_decode_split_v16 / _attention_v16: as the K16/V8 calls,
+ *     with v_cache16 in place of (v_cache, v_scale).  Within a 16-token page
+ *     the P.V products are summed in fp16, so |v| must stay below 4,094.
+ */
+int32_t k16v8_kv_append_v16(const void *k, int64_t k_token_stride, const void *v,
+                            int64_t v_token_stride, const int64_t *slot_mapping,
+                            int32_t num_tokens, void *k_cache, void *v_cache16,
+                            int32_t num_pages, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t *dev_error, void *stream);
+
+int32_t k16v8_paged_decode_split_v16(const void *q, const void *k_cache, const void *v_cache16,
+                                     const int32_t *block_table, int32_t max_pages_per_seq,
+                                     const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+                                     int32_t num_qo_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t num_pages, float sm_scale,
+                                     int32_t split_chunk, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_error, void *stream);
+
+int32_t k16v8_paged_decode_attention_v16(const void *q, const void *k_cache,
+                                         const void *v_cache16, const int32_t *block_table,
+                                         int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                         int32_t max_seq_len, int32_t batch,
+                                         int32_t num_qo_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t num_pages, float sm_scale,
+                                         int32_t split_chunk, void *workspace,
+                                         size_t workspace_bytes, void *out, float *lse,
+                                         int32_t *dev_error, void *stream);
+
+/*
  * paged_prefill_attention -- causal attention of a chunk of new prompt tokens
  * against the paged cache, on tensor cores.  The page's throughput metric
  * includes prefill ("Fixed throughput studies"); its 8K profile admits fresh

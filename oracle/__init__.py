@@ -70,6 +70,11 @@ def _load():
                                                 i32, i32, i32, f64, i32, i32, P, P, P,
                                                 P, i32]
             lib.k16v8o_paged_decode.restype = ctypes.c_int
+            lib.k16v8o_paged_decode_v16.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32,
+                                                    i32, i32, f64, P, P, i32]
+            lib.k16v8o_paged_decode_v16.restype = ctypes.c_int
+            lib.k16v8o_kv_append_v16.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32]
+            lib.k16v8o_kv_append_v16.restype = ctypes.c_int
             lib.k16v8o_merge.argtypes = [P, P, P, i32, i32, i32, i32, P, P]
             lib.k16v8o_merge.restype = ctypes.c_int
             lib.k16v8o_paged_prefill.argtypes = [P, P, i32, P, P, P, P, i32, P, i32,
@@ -209,6 +214,36 @@ def paged_decode(q, k_cache, v_cache, v_scale, block_table, seq_lens, sm_scale,
         split_chunk, C, _ptr(out), _ptr(lse), _ptr(po), _ptr(pl), nthreads)
     _check(rc, "paged_decode")
     return res
+
+
+def kv_append_v16(k, v, slot_mapping, k_cache, v_cache16, page_size: int = 16) -> None:
+    """FP16-KV control cache write: K and V copied (v fp16 [T, Hkv, D])."""
+    T, Hkv, D = k.shape
+    kb, vb = _bits16(k), _bits16(np.asarray(v).astype(np.float16))
+    sm = np.ascontiguousarray(slot_mapping, np.int64)
+    rc = _load().k16v8o_kv_append_v16(_ptr(kb), _ptr(vb), _ptr(sm), T,
+                                      _ptr(k_cache.view(np.uint16)),
+                                      _ptr(v_cache16.view(np.uint16)), k_cache.shape[0], Hkv, D,
+                                      page_size)
+    _check(rc, "kv_append_v16")
+
+
+def paged_decode_v16(q, k_cache, v_cache16, block_table, seq_lens, sm_scale, page_size=16,
+                     nthreads: int = 0):
+    """FP16-KV control: exact attention over a cache with fp16 values."""
+    qb = _bits16(q)
+    B, Hq, D = q.shape
+    P, Hkv = k_cache.shape[:2]
+    bt = np.ascontiguousarray(block_table, np.int32)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = _load().k16v8o_paged_decode_v16(
+        _ptr(qb), _ptr(k_cache.view(np.uint16)), _ptr(v_cache16.view(np.uint16)), _ptr(bt),
+        bt.shape[1], _ptr(sl), B, Hq, Hkv, D, page_size, P, float(sm_scale), _ptr(out),
+        _ptr(lse), nthreads)
+    _check(rc, "paged_decode_v16")
+    return out, lse
 
 
 def merge(partial_o: np.ndarray, partial_lse: np.ndarray, n_chunks: np.ndarray):

@@ -198,7 +198,7 @@ int k16v8o_kv_append(const uint16_t *k, int64_t k_ts, const void *v,
  * the sum of exp(score)); writes the normalised output into out[D].
  * Returns ERR_BOUNDS through *err for page ids outside [0, num_pages). */
 static double attend_range(const uint16_t *qrow, const uint16_t *k_cache,
-                           const uint8_t *v_cache, double vscale,
+                           const void *v_cache, int v_f16, double vscale,
                            const int32_t *btab, int32_t g, int32_t Hkv,
                            int32_t D, int32_t page_size, int32_t num_pages,
                            double sm_scale, int64_t lo, int64_t hi,
@@ -234,7 +234,8 @@ static double attend_range(const uint16_t *qrow, const uint16_t *k_cache,
         double p = exp(s_buf[j - lo] - m);
         l += p;
         for (int32_t d = 0; d < D; ++d)
-            out[d] += p * (vscale * k16v8o_e4m3_to_double(v_cache[base + d]));
+            out[d] += p * (v_f16 ? k16v8o_half_to_double(((const uint16_t *)v_cache)[base + d])
+                                 : vscale * k16v8o_e4m3_to_double(((const uint8_t *)v_cache)[base + d]));
     }
     for (int32_t d = 0; d < D; ++d)
         out[d] /= l;
@@ -302,7 +303,8 @@ static int run_parallel(int (*fn)(void *, int64_t, double *), void *ctx,
 
 typedef struct {
     const uint16_t *q, *k_cache;
-    const uint8_t *v_cache;
+    const void *v_cache;
+    int v_f16;
     const float *v_scale;
     const int32_t *block_table, *seq_lens;
     int32_t max_pages, Hq, Hkv, D, page_size, num_pages;
@@ -323,9 +325,9 @@ static int decode_item(void *vctx, int64_t item, double *scratch)
     int err = OK;
     if (L < 0 || (L + c->page_size - 1) / c->page_size > c->max_pages)
         return ERR_ARG;
-    double vs = (double)c->v_scale[g];
+    double vs = c->v_f16 ? 1.0 : (double)c->v_scale[g];
     if (c->out) {
-        double l = attend_range(qrow, c->k_cache, c->v_cache, vs, btab, g,
+        double l = attend_range(qrow, c->k_cache, c->v_cache, c->v_f16, vs, btab, g,
                                 c->Hkv, c->D, c->page_size, c->num_pages,
                                 c->sm_scale, 0, L, c->out + (b * c->Hq + h) * c->D,
                                 scratch, &err);
@@ -338,7 +340,7 @@ static int decode_item(void *vctx, int64_t item, double *scratch)
             int64_t lo = (int64_t)ch * c->split_chunk;
             int64_t hi = lo + c->split_chunk < L ? lo + c->split_chunk : L;
             int64_t idx = (b * c->Hq + h) * c->max_chunks + ch;
-            double l = attend_range(qrow, c->k_cache, c->v_cache, vs, btab, g,
+            double l = attend_range(qrow, c->k_cache, c->v_cache, c->v_f16, vs, btab, g,
                                     c->Hkv, c->D, c->page_size, c->num_pages,
                                     c->sm_scale, lo, hi, c->partial_o + idx * c->D,
                                     scratch, &err);
@@ -348,6 +350,27 @@ static int decode_item(void *vctx, int64_t item, double *scratch)
         }
     }
     return OK;
+}
+
+static int paged_decode_impl(const uint16_t *q, const uint16_t *k_cache, const void *v_cache,
+                             int v_f16, const float *v_scale, const int32_t *block_table,
+                             int32_t max_pages, const int32_t *seq_lens, int32_t B, int32_t Hq,
+                             int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                             double sm_scale, int32_t split_chunk, int32_t max_chunks,
+                             double *out, double *lse, double *partial_o, double *partial_lse,
+                             int32_t nthreads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || D > 512 ||
+        page_size <= 0)
+        return ERR_ARG;
+    int64_t maxL = 0;
+    for (int32_t b = 0; b < B; ++b)
+        if (seq_lens[b] > maxL)
+            maxL = seq_lens[b];
+    decode_ctx c = {q, k_cache, v_cache, v_f16, v_scale, block_table, seq_lens,
+                    max_pages, Hq, Hkv, D, page_size, num_pages, sm_scale,
+                    split_chunk, max_chunks, out, lse, partial_o, partial_lse};
+    return run_parallel(decode_item, &c, (int64_t)B * Hq, maxL, nthreads);
 }
 
 /* q: fp16 bits [B][Hq][D]; caches as in kv_append; block_table int32
@@ -363,17 +386,49 @@ int k16v8o_paged_decode(const uint16_t *q, const uint16_t *k_cache,
                         int32_t max_chunks, double *out, double *lse,
                         double *partial_o, double *partial_lse, int32_t nthreads)
 {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || D > 512 ||
-        page_size <= 0)
+    return paged_decode_impl(q, k_cache, v_cache, 0, v_scale, block_table, max_pages, seq_lens,
+                             B, Hq, Hkv, D, page_size, num_pages, sm_scale, split_chunk,
+                             max_chunks, out, lse, partial_o, partial_lse, nthreads);
+}
+
+/* The FP16-KV control: the same attention over a cache whose values are
+ * stored as fp16 (no quantisation, no scale). */
+int k16v8o_paged_decode_v16(const uint16_t *q, const uint16_t *k_cache,
+                            const uint16_t *v_cache16, const int32_t *block_table,
+                            int32_t max_pages, const int32_t *seq_lens, int32_t B,
+                            int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                            int32_t num_pages, double sm_scale, double *out, double *lse,
+                            int32_t nthreads)
+{
+    return paged_decode_impl(q, k_cache, v_cache16, 1, NULL, block_table, max_pages, seq_lens,
+                             B, Hq, Hkv, D, page_size, num_pages, sm_scale, 0, 0, out, lse,
+                             NULL, NULL, nthreads);
+}
+
+/* FP16-KV control cache write: K and V copied as fp16. */
+int k16v8o_kv_append_v16(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
+                         int32_t T, uint16_t *k_cache, uint16_t *v_cache16, int32_t num_pages,
+                         int32_t Hkv, int32_t D, int32_t page_size)
+{
+    if (T < 0 || Hkv <= 0 || D <= 0 || page_size <= 0 || num_pages < 0)
         return ERR_ARG;
-    int64_t maxL = 0;
-    for (int32_t b = 0; b < B; ++b)
-        if (seq_lens[b] > maxL)
-            maxL = seq_lens[b];
-    decode_ctx c = {q, k_cache, v_cache, v_scale, block_table, seq_lens,
-                    max_pages, Hq, Hkv, D, page_size, num_pages, sm_scale,
-                    split_chunk, max_chunks, out, lse, partial_o, partial_lse};
-    return run_parallel(decode_item, &c, (int64_t)B * Hq, maxL, nthreads);
+    int64_t nslots = (int64_t)num_pages * page_size;
+    for (int32_t t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= nslots)
+            return ERR_BOUNDS;
+        int64_t page = slot / page_size, off = slot % page_size;
+        for (int32_t h = 0; h < Hkv; ++h)
+            for (int32_t d = 0; d < D; ++d) {
+                int64_t dst = ((page * Hkv + h) * page_size + off) * D + d;
+                int64_t src = ((int64_t)t * Hkv + h) * D + d;
+                k_cache[dst] = k[src];
+                v_cache16[dst] = v[src];
+            }
+    }
+    return OK;
 }
 
 /* ---- log-sum-exp merge of split partials ------------------------------- */
@@ -451,7 +506,7 @@ static int prefill_item(void *vctx, int64_t item, double *scratch)
     int32_t g = h / (c->Hq / c->Hkv);
     int err = OK;
     double l = attend_range(c->q + (row * c->Hq + h) * c->D, c->k_cache,
-                            c->v_cache, (double)c->v_scale[g],
+                            c->v_cache, 0, (double)c->v_scale[g],
                             c->block_table + (int64_t)b * c->max_pages, g,
                             c->Hkv, c->D, c->page_size, c->num_pages,
                             c->sm_scale, 0, pos + 1,

@@ -231,3 +231,23 @@ def test_prefill_chunked_equals_unchunked():
                                 a.prompt_lens, a.sm_scale)
     for r in range(a.q.shape[0]):
         assert np.array_equal(full_o[r][0], o[r]) and np.array_equal(full_o[r][1], l[r])
+
+
+def test_fp16_kv_control_decode_matches_library_sdpa():
+    """FP16-KV control (values stored exactly in fp16): placement and
+    attention pinned to numpy indexing and torch SDPA."""
+    w = workloads.make_decode("v16", 12, [45, 130], num_qo_heads=8, num_kv_heads=2, num_pages=20)
+    v16 = w.v_tok.astype(np.float16)
+    kc = np.full((w.num_pages, 2, 16, 128), 0x7E00, np.uint16).view(np.float16)
+    vc = np.full((w.num_pages, 2, 16, 128), 0x7E00, np.uint16).view(np.float16)
+    oracle.kv_append_v16(w.k_tok, v16, w.slot_mapping, kc, vc)
+    page, off = w.slot_mapping // 16, w.slot_mapping % 16
+    assert np.array_equal(vc[page, :, off, :].view(np.uint16), v16.view(np.uint16))
+    out, lse = oracle.paged_decode_v16(w.q, kc, vc, w.block_table, w.seq_lens, w.sm_scale)
+    for b in range(w.batch):
+        lo, hi = seq_rows(w.seq_lens)[b]
+        k = w.k_tok[lo:hi].astype(np.float64).transpose(1, 0, 2)
+        v = v16[lo:hi].astype(np.float64).transpose(1, 0, 2)
+        ro, rl = sdpa_reference(w.q[b].astype(np.float64)[:, None, :], k, v, w.sm_scale)
+        np.testing.assert_allclose(out[b], ro[:, 0], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse[b], rl[:, 0], rtol=1e-12, atol=1e-12)
