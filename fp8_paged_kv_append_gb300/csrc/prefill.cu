@@ -58,7 +58,9 @@ constexpr uint32_t kOffK = 2 * kQBytes;            // 2 stages
 constexpr uint32_t kOffVst = kOffK + 2 * kKStage;  // 2 stages
 constexpr uint32_t kOffV = kOffVst + 2 * kVstStage;  // 2 stages
 constexpr uint32_t kOffP = kOffV + 2 * kVStage;    // P_A, P_B
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr int kMaxIdPages = 1024;                  // page ids staged in shared memory
+constexpr uint32_t kOffIds = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffBar = kOffIds + kMaxIdPages * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256;
 constexpr uint32_t kTmemCols = 512;  // S_A [0,64) S_B [64,128) O_A [128,256) O_B [256,384)
 
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   uint8_t *sVst = base + kOffVst;
   uint8_t *sV = base + kOffV;
   uint8_t *sP = base + kOffP;
+  int *page_ids = reinterpret_cast<int *>(base + kOffIds);
   uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kOffBar + kNumBars * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kOffBar + kNumBars * 8 + 4);
@@ -166,18 +169,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     for (int j = 0; j < n_kv; ++j) {
       cta_wait(&bars[kBarSFull + w], j & 1, abort_flag, dev_error);
       tc::fence_after_sync();
-      const bool need_mask = j * kKv + kKv - 1 > p_lo;
+      const bool need_mask = j * kKv + kKv - 1 > p_lo;  // diagonal tile
       const int lim = p_r - j * kKv;  // last visible column of this tile
       uint32_t sr[2][32];
       tc::tmem_ld32(tS + lane_base, sr[0]);
       tc::tmem_ld32(tS + lane_base + 32, sr[1]);
       tc::tmem_wait_ld();
       float rmax = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (!need_mask || c * 32 + e <= lim) rmax = fmaxf(rmax, __uint_as_float(sr[c][e]));
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e <= lim) rmax = fmaxf(rmax, __uint_as_float(sr[c][e]));
+      } else {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[c][e]));
+        rmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      }
       rmax *= qk_scale;
       float alpha = 1.f;
       if (rmax > m_used + 8.f) {
@@ -200,7 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         }
         tc::tmem_wait_st();
       }
-      float psum = 0.f;
+      // p = 2^(s*scale - m) in pairs; fp32 row sum for the LSE, fp16 P tile
+      const float2 sc2 = make_float2(qk_scale, qk_scale);
+      const float2 nm2 = make_float2(-m_used, -m_used);
+      float2 ps2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
@@ -209,12 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c0 = c * 32 + q * 8 + 2 * e;
-            float p0 = ex2(fmaf(__uint_as_float(sr[c][q * 8 + 2 * e]), qk_scale, -m_used));
-            float p1 = ex2(fmaf(__uint_as_float(sr[c][q * 8 + 2 * e + 1]), qk_scale, -m_used));
-            if (need_mask && c0 > lim) p0 = 0.f;
-            if (need_mask && c0 + 1 > lim) p1 = 0.f;
-            psum += p0 + p1;
-            const __half2 h = __floats2half2_rn(p0, p1);
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][q * 8 + 2 * e]),
+                                                    __uint_as_float(sr[c][q * 8 + 2 * e + 1])),
+                                        sc2, nm2);
+            float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            if (need_mask) {
+              if (c0 > lim) pp.x = 0.f;
+              if (c0 + 1 > lim) pp.y = 0.f;
+            }
+            ps2 = __fadd2_rn(ps2, pp);
+            const __half2 h = __floats2half2_rn(pp.x, pp.y);
             pk[e] = *reinterpret_cast<const uint32_t *>(&h);
           }
           const uint32_t off = r * 128 + (c * 32 + q * 8) * 2;
@@ -222,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
+      const float psum = ps2.x + ps2.y;
       l = l * alpha + psum;
       fence_proxy_async();
       tc::fence_before_sync();
@@ -294,6 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
   } else if (warp == kLoadWarp) {
     // ================= loads =================
+    // stage this pair's page ids in shared memory (lane-parallel)
+    const int n_ids = min(n_kv * kPagesPerTile, (L + kPage - 1) / kPage);
+    for (int i = lane; i < min(n_ids, kMaxIdPages); i += 32) {
+      const int p = __ldg(bt + i);
+      page_ids[i] = (p >= 0 && p < num_pages) ? p : -1;
+      if (p < 0 || p >= num_pages) flag_error(dev_error, K16V8_DEVERR_PAGE);
+    }
+    __syncwarp();
     if (lane == 0) {
       tc::prefetch_tensormap(&tmap_q);
       tc::prefetch_tensormap(&tmap_k);
@@ -317,12 +345,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         for (int i = 0; i < kPagesPerTile; ++i) {
           pid[i] = -1;
           if (i < live) {
-            const int p = __ldg(bt + j * kPagesPerTile + i);
-            if (p >= 0 && p < num_pages) {
+            const int pi = j * kPagesPerTile + i;
+            int p;
+            if (pi < kMaxIdPages) {
+              p = page_ids[pi];
+            } else {
+              p = __ldg(bt + pi);
+              if (p < 0 || p >= num_pages) {
+                flag_error(dev_error, K16V8_DEVERR_PAGE);
+                p = -1;
+              }
+            }
+            if (p >= 0) {
               pid[i] = p;
               kbytes += 2 * 2048;
-            } else {
-              flag_error(dev_error, K16V8_DEVERR_PAGE);
             }
           }
         }
