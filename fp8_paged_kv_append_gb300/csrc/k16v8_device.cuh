@@ -72,6 +72,41 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   return false;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// try_wait with an explicit suspend-time hint (ns) for latency-critical
+// hand-offs.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded spin on test_wait (no suspension): for waits on the critical path
+// of a pipeline.  The bound is far beyond any real copy or MMA.
+constexpr uint32_t kMaxSpins = 1u << 28;
+__device__ __forceinline__ bool mbar_spin_bounded(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kMaxSpins; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return false;
+}
+
 // One contiguous global->shared copy on the bulk-async engine, completing
 // `bytes` of transaction count on `bar`.  dst, src 16-B aligned; bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
