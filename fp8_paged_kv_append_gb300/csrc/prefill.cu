@@ -17,12 +17,12 @@
 //    than 2^8, otherwise the stale max is kept -- exact, as the final
 //    normalisation uses the same max), P (fp16) into a K-major SW128 tile;
 //    finally O / l * v_scale -> fp16 and the LSE.
-//  * warps 8-9: V dequantisation, E4M3 pages -> fp16 MN-major SW128 tile
+//  * warps 8-11: V dequantisation, E4M3 pages -> fp16 MN-major SW128 tile
 //    (hardware cvt).
-//  * warp 10: loads -- Q by TMA (3-D box: 64 dims x 4 heads x 32 tokens),
+//  * warp 12: loads -- Q by TMA (3-D box: 64 dims x 4 heads x 32 tokens),
 //    K pages by TMA straight into the K-major SW128 operand layout, E4M3 V
 //    pages by bulk copy; two stages each.
-//  * warp 11: one thread issues every tcgen05.mma (kind::f16, fp32
+//  * warp 13: one thread issues every tcgen05.mma (kind::f16, fp32
 //    accumulators in tensor memory: S_A, S_B 64 columns each, O_A, O_B 128
 //    each) in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...,
 //    so one tile's softmax overlaps the other tile's MMAs.
@@ -43,9 +43,9 @@ constexpr int kQTok = 32;                   // query tokens per tile
 constexpr int kRows = kQTok * kGroup;       // 128 MMA rows per tile
 constexpr int kKv = 64;                     // KV positions per tile
 constexpr int kPagesPerTile = kKv / kPage;  // 4
-constexpr int kDequantWarps = 2;
-constexpr int kLoadWarp = 10, kMmaWarp = 11;
-constexpr int kThreads = 12 * 32;
+constexpr int kDequantWarps = 4;
+constexpr int kLoadWarp = 12, kMmaWarp = 13;
+constexpr int kThreads = 14 * 32;
 
 constexpr uint32_t kQBytes = kRows * 256;          // one Q tile: 2 K-blocks [128][64] fp16
 constexpr uint32_t kKBlk = kKv * 128;              // [64 pos][64 dims] fp16
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
   } else if (warp < 8 + kDequantWarps) {
     // ================= V dequantisation =================
-    const int dt = tid - 8 * 32;  // 0 .. 63
+    const int dt = tid - 8 * 32;  // 0 .. 127
     for (int j = 0; j < n_kv; ++j) {
       const int s = j & 1;
       cta_wait(&bars[kBarVstFull + s], (j >> 1) & 1, abort_flag, dev_error);
@@ -389,28 +389,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     if (lane == 0) {
       constexpr uint32_t kIdescQK = tc::idesc_f16_f32(kRows, kKv, false, false);
       constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kRows, kHeadDim, false, true);
+      // Descriptors of every operand tile, built once; an MMA's operand is
+      // its tile's descriptor plus a constant step in the start-address
+      // field (16-byte units): +2 per 16 fp16 along K inside a 128-byte
+      // row, +kKBlk/16 (or kQBytes/32) per 64-element K-block, +128 per
+      // 16 positions of the MN-major V tile.
+      const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t dq1 = tc::smem_desc_sw128(smem_addr(sQ + kQBytes), 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(sK), 16, 1024);
+      const uint64_t dk1 = tc::smem_desc_sw128(smem_addr(sK + kKStage), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(sV), kKBlk, 1024);
+      const uint64_t dv1 = tc::smem_desc_sw128(smem_addr(sV + kVStage), kKBlk, 1024);
+      const uint64_t dp0 = tc::smem_desc_sw128(smem_addr(sP), 16, 1024);
+      const uint64_t dp1 = tc::smem_desc_sw128(smem_addr(sP + kPBytes), 16, 1024);
       auto issue_s = [&](int w, int j) {
-        const uint8_t *k_st = sK + (j & 1) * kKStage;
-        const uint8_t *q_t = sQ + w * kQBytes;
+        const uint64_t a0 = w ? dq1 : dq0, b0 = (j & 1) ? dk1 : dk0;
+        const uint32_t d = tmem + w * 64;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = tc::smem_desc_sw128(
-              smem_addr(q_t + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32), 16, 1024);
-          const uint64_t bd =
-              tc::smem_desc_sw128(smem_addr(k_st + (kk >> 2) * kKBlk + (kk & 3) * 32), 16, 1024);
-          tc::mma_f16_ss(tmem + w * 64, ad, bd, kIdescQK, kk > 0);
+          const uint64_t ao = static_cast<uint64_t>((kk >> 2) * (kQBytes / 2 / 16) + (kk & 3) * 2);
+          const uint64_t bo = static_cast<uint64_t>((kk >> 2) * (kKBlk / 16) + (kk & 3) * 2);
+          tc::mma_f16_ss(d, a0 + ao, b0 + bo, kIdescQK, kk > 0);
         }
         tc::mma_commit(&bars[kBarSFull + w]);
       };
       auto issue_pv = [&](int w, int j) {
-        const uint8_t *v_st = sV + (j & 1) * kVStage;
-        const uint8_t *p_t = sP + w * kPBytes;
+        const uint64_t a0 = w ? dp1 : dp0, b0 = (j & 1) ? dv1 : dv0;
+        const uint32_t d = tmem + 128 + w * 128;
+        const bool acc0 = j > 0;
 #pragma unroll
-        for (int kk = 0; kk < kKv / 16; ++kk) {
-          const uint64_t ad = tc::smem_desc_sw128(smem_addr(p_t + kk * 32), 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(smem_addr(v_st + kk * 2048), kKBlk, 1024);
-          tc::mma_f16_ss(tmem + 128 + w * 128, ad, bd, kIdescPV, j > 0 || kk > 0);
-        }
+        for (int kk = 0; kk < kKv / 16; ++kk)
+          tc::mma_f16_ss(d, a0 + static_cast<uint64_t>(kk * 2), b0 + static_cast<uint64_t>(kk * 128),
+                         kIdescPV, acc0 || kk > 0);
         tc::mma_commit(&bars[kBarODone + w]);
       };
       cta_wait(&bars[kBarQ], 0, abort_flag, dev_error);
