@@ -9,23 +9,26 @@
 //
 // One CTA per (pair of 32-token query tiles, KV head, sequence), one CTA per
 // SM.  The 4 query heads of the GQA group are packed into the 128 rows of a
-// tile (row = token*4 + head); both tiles (A, B) share every K/V tile.
-// Warp roles:
-//  * warps 0-3 / 4-7: softmax of tile A / B, one thread per row: load the S
-//    row from tensor memory, causal mask, log2-domain scale, running max
-//    (the O row in tensor memory is rescaled only when the max grows by more
-//    than 2^8, otherwise the stale max is kept -- exact, as the final
-//    normalisation uses the same max), P (fp16) into a K-major SW128 tile;
+// tile (row = token*4 + head); both tiles (A, B) share every 128-position
+// K/V tile.  Tensor memory (512 columns): S_A, S_B (128 fp32 columns each;
+// P, fp16, is written over the first 64 columns of its S), O_A, O_B (128
+// each).  Warp roles:
+//  * warps 0-3 / 4-7: softmax of tile A / B, one thread per row: S row from
+//    tensor memory, causal mask, log2-domain scale, running max (the O row in
+//    tensor memory is rescaled only when the max grows by more than 2^8,
+//    otherwise the stale max is kept -- exact, as the final normalisation
+//    uses the same max), fp32 row sum, P (fp16) back into tensor memory;
 //    finally O / l * v_scale -> fp16 and the LSE.
-//  * warps 8-11: V dequantisation, E4M3 pages -> fp16 MN-major SW128 tile
-//    (hardware cvt).
+//  * warps 8-11: V dequantisation, E4M3 pages -> fp16 MN-major SW128 tile.
 //  * warp 12: loads -- Q by TMA (3-D box: 64 dims x 4 heads x 32 tokens),
 //    K pages by TMA straight into the K-major SW128 operand layout, E4M3 V
 //    pages by bulk copy; two stages each.
 //  * warp 13: one thread issues every tcgen05.mma (kind::f16, fp32
-//    accumulators in tensor memory: S_A, S_B 64 columns each, O_A, O_B 128
-//    each) in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...,
-//    so one tile's softmax overlaps the other tile's MMAs.
+//    accumulators): S = Q K^T with both operands in shared memory, O += P V
+//    with P read from tensor memory; order S_A(0) S_B(0) | PV_A(j) S_A(j+1)
+//    PV_B(j) S_B(j+1) ..., so one tile's softmax overlaps the other tile's
+//    MMAs.  The MMAs of one thread execute in issue order, so S_w(j+1) lands
+//    after PV_w(j) has read P_w(j) from the same columns.
 // Every hand-off is an mbarrier (transaction counts for copies,
 // tcgen05.commit for MMAs, thread arrivals for softmax and dequant); every
 // wait is bounded.
@@ -41,28 +44,26 @@ namespace prefill {
 
 constexpr int kQTok = 32;                   // query tokens per tile
 constexpr int kRows = kQTok * kGroup;       // 128 MMA rows per tile
-constexpr int kKv = 64;                     // KV positions per tile
-constexpr int kPagesPerTile = kKv / kPage;  // 4
+constexpr int kKv = 128;                    // KV positions per tile
+constexpr int kPagesPerTile = kKv / kPage;  // 8
 constexpr int kDequantWarps = 4;
 constexpr int kLoadWarp = 12, kMmaWarp = 13;
 constexpr int kThreads = 14 * 32;
 
 constexpr uint32_t kQBytes = kRows * 256;          // one Q tile: 2 K-blocks [128][64] fp16
-constexpr uint32_t kKBlk = kKv * 128;              // [64 pos][64 dims] fp16
+constexpr uint32_t kKBlk = kKv * 128;              // [128 pos][64 dims] fp16
 constexpr uint32_t kKStage = 2 * kKBlk;
-constexpr uint32_t kVstStage = kKv * 128;          // [64 pos][128] E4M3
-constexpr uint32_t kVStage = 2 * kKBlk;            // 2 MN-blocks [64 pos][64] fp16
-constexpr uint32_t kPBytes = kRows * 128;          // [128 rows][64] fp16
+constexpr uint32_t kVstStage = kKv * 128;          // [128 pos][128] E4M3
+constexpr uint32_t kVStage = 2 * kKBlk;            // 2 MN-blocks [128 pos][64] fp16
 constexpr uint32_t kOffQ = 0;                      // Q_A, Q_B
 constexpr uint32_t kOffK = 2 * kQBytes;            // 2 stages
 constexpr uint32_t kOffVst = kOffK + 2 * kKStage;  // 2 stages
 constexpr uint32_t kOffV = kOffVst + 2 * kVstStage;  // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kVStage;    // P_A, P_B
-constexpr int kMaxIdPages = 1024;                  // page ids staged in shared memory
-constexpr uint32_t kOffIds = kOffP + 2 * kPBytes;
+constexpr int kMaxIdPages = 512;                   // page ids staged in shared memory
+constexpr uint32_t kOffIds = kOffV + 2 * kVStage;
 constexpr uint32_t kOffBar = kOffIds + kMaxIdPages * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256;
-constexpr uint32_t kTmemCols = 512;  // S_A [0,64) S_B [64,128) O_A [128,256) O_B [256,384)
+constexpr uint32_t kTmemCols = 512;  // S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512)
 
 enum {
   kBarQ = 0,
@@ -103,7 +104,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   uint8_t *sK = base + kOffK;
   uint8_t *sVst = base + kOffVst;
   uint8_t *sV = base + kOffV;
-  uint8_t *sP = base + kOffP;
   int *page_ids = reinterpret_cast<int *>(base + kOffIds);
   uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kOffBar + kNumBars * 8);
@@ -162,33 +162,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const int p_r = row_valid ? pos0 + t_abs : 0;
     const float qk_scale = sm_scale * kLog2e;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + w * 64;
-    const uint32_t tO = tmem + 128 + w * 128;
-    uint8_t *p_tile = sP + w * kPBytes;
+    const uint32_t tS = tmem + w * 128;   // S_w; P_w in its first 64 columns
+    const uint32_t tO = tmem + 256 + w * 128;
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < n_kv; ++j) {
       cta_wait(&bars[kBarSFull + w], j & 1, abort_flag, dev_error);
       tc::fence_after_sync();
       const bool need_mask = j * kKv + kKv - 1 > p_lo;  // diagonal tile
       const int lim = p_r - j * kKv;  // last visible column of this tile
-      uint32_t sr[2][32];
-      tc::tmem_ld32(tS + lane_base, sr[0]);
-      tc::tmem_ld32(tS + lane_base + 32, sr[1]);
-      tc::tmem_wait_ld();
+      // pass 1: row max (64 columns per load round)
       float rmax = -INFINITY;
-      if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sr[2][32];
+        tc::tmem_ld32(tS + lane_base + h * 64, sr[0]);
+        tc::tmem_ld32(tS + lane_base + h * 64 + 32, sr[1]);
+        tc::tmem_wait_ld();
+        if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e <= lim) rmax = fmaxf(rmax, __uint_as_float(sr[c][e]));
-      } else {
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+            for (int e = 0; e < 32; ++e)
+              if (h * 64 + c * 32 + e <= lim) rmax = fmaxf(rmax, __uint_as_float(sr[c][e]));
+        } else {
+          float m4[4] = {rmax, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[c][e]));
-        rmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[c][e]));
+          rmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
       }
       rmax *= qk_scale;
       float alpha = 1.f;
@@ -196,11 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         alpha = ex2(m_used - rmax);
         m_used = rmax;
       }
-      // P_w and O_w are free once PV_w(j-1) has completed
+      // O_w is stable once PV_w(j-1) has completed
       if (j > 0) cta_wait(&bars[kBarODone + w], (j - 1) & 1, abort_flag, dev_error);
       tc::fence_after_sync();
-      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-      if (rescale) {
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -210,22 +212,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tc::tmem_st32(tO + lane_base + c * 32, o);
         }
-        tc::tmem_wait_st();
       }
-      // p = 2^(s*scale - m) in pairs; fp32 row sum for the LSE, fp16 P tile
+      // pass 2: p = 2^(s*scale - m) in pairs; fp32 row sum; P (fp16) over the
+      // already-read S columns: positions 64h.. land in P columns 32h..
       const float2 sc2 = make_float2(qk_scale, qk_scale);
       const float2 nm2 = make_float2(-m_used, -m_used);
       float2 ps2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sr[2][32];
+        tc::tmem_ld32(tS + lane_base + h * 64, sr[0]);
+        tc::tmem_ld32(tS + lane_base + h * 64 + 32, sr[1]);
+        tc::tmem_wait_ld();
+        uint32_t pk[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // 8 values -> one 16-byte chunk of P
-          uint32_t pk[4];
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c0 = c * 32 + q * 8 + 2 * e;
-            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][q * 8 + 2 * e]),
-                                                    __uint_as_float(sr[c][q * 8 + 2 * e + 1])),
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = h * 64 + c * 32 + 2 * e;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * e]),
+                                                    __uint_as_float(sr[c][2 * e + 1])),
                                         sc2, nm2);
             float2 pp = make_float2(ex2(x.x), ex2(x.y));
             if (need_mask) {
@@ -233,17 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
               if (c0 + 1 > lim) pp.y = 0.f;
             }
             ps2 = __fadd2_rn(ps2, pp);
-            const __half2 h = __floats2half2_rn(pp.x, pp.y);
-            pk[e] = *reinterpret_cast<const uint32_t *>(&h);
+            const __half2 hh = __floats2half2_rn(pp.x, pp.y);
+            pk[c * 16 + e] = *reinterpret_cast<const uint32_t *>(&hh);
           }
-          const uint32_t off = r * 128 + (c * 32 + q * 8) * 2;
-          *reinterpret_cast<uint4 *>(p_tile + tc::sw128(off)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        tc::tmem_st32(tS + lane_base + h * 32, pk);
       }
-      const float psum = ps2.x + ps2.y;
-      l = l * alpha + psum;
-      fence_proxy_async();
+      tc::tmem_wait_st();
+      l = l * alpha + (ps2.x + ps2.y);
       tc::fence_before_sync();
       mbar_arrive(&bars[kBarPFull + w]);
     }
@@ -264,9 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             uint32_t pk[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const __half2 h = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
-                                                  __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
-              pk[e] = *reinterpret_cast<const uint32_t *>(&h);
+              const __half2 hh = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
+                                                   __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
+              pk[e] = *reinterpret_cast<const uint32_t *>(&hh);
             }
             *reinterpret_cast<uint4 *>(out + orow * kHeadDim + c * 32 + q * 8) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
   } else if (warp < 8 + kDequantWarps) {
     // ================= V dequantisation =================
-    const int dt = tid - 8 * 32;  // 0 .. 127
+    const int dt = tid - 8 * 32;  // 0 .. 32 * kDequantWarps - 1
     for (int j = 0; j < n_kv; ++j) {
       const int s = j & 1;
       cta_wait(&bars[kBarVstFull + s], (j >> 1) & 1, abort_flag, dev_error);
@@ -400,11 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       const uint64_t dk1 = tc::smem_desc_sw128(smem_addr(sK + kKStage), 16, 1024);
       const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(sV), kKBlk, 1024);
       const uint64_t dv1 = tc::smem_desc_sw128(smem_addr(sV + kVStage), kKBlk, 1024);
-      const uint64_t dp0 = tc::smem_desc_sw128(smem_addr(sP), 16, 1024);
-      const uint64_t dp1 = tc::smem_desc_sw128(smem_addr(sP + kPBytes), 16, 1024);
       auto issue_s = [&](int w, int j) {
         const uint64_t a0 = w ? dq1 : dq0, b0 = (j & 1) ? dk1 : dk0;
-        const uint32_t d = tmem + w * 64;
+        const uint32_t d = tmem + w * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ao = static_cast<uint64_t>((kk >> 2) * (kQBytes / 2 / 16) + (kk & 3) * 2);
@@ -414,13 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         tc::mma_commit(&bars[kBarSFull + w]);
       };
       auto issue_pv = [&](int w, int j) {
-        const uint64_t a0 = w ? dp1 : dp0, b0 = (j & 1) ? dv1 : dv0;
-        const uint32_t d = tmem + 128 + w * 128;
+        const uint64_t b0 = (j & 1) ? dv1 : dv0;
+        const uint32_t a = tmem + w * 128;  // P_w: 8 columns per 16 positions
+        const uint32_t d = tmem + 256 + w * 128;
         const bool acc0 = j > 0;
 #pragma unroll
         for (int kk = 0; kk < kKv / 16; ++kk)
-          tc::mma_f16_ss(d, a0 + static_cast<uint64_t>(kk * 2), b0 + static_cast<uint64_t>(kk * 128),
-                         kIdescPV, acc0 || kk > 0);
+          tc::mma_f16_ts(d, a + kk * 8, b0 + static_cast<uint64_t>(kk * 128), kIdescPV,
+                         acc0 || kk > 0);
         tc::mma_commit(&bars[kBarODone + w]);
       };
       cta_wait(&bars[kBarQ], 0, abort_flag, dev_error);
