@@ -83,9 +83,11 @@ enum {
 // CTA-wide abort flag (and the device error word); later waits return at
 // once, so every role runs to the end of its loop.
 __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                         int32_t *dev_error) {
+                                         int32_t *dev_error, bool spin = false) {
   if (*abort_flag) return false;
-  if (mbar_wait_bounded(bar, parity)) return true;
+  // The single-thread MMA and load roles spin (no suspension, so a hand-off
+  // is seen at once); the many-thread roles suspend between polls.
+  if (spin ? mbar_spin_bounded(bar, parity) : mbar_wait_bounded(bar, parity)) return true;
   *abort_flag = 1;
   flag_error(dev_error, K16V8_DEVERR_TIMEOUT);
   return false;
@@ -338,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       for (int j = 0; j < n_kv; ++j) {
         const int s = j & 1;
         if (j >= 2) {
-          cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error);
-          cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error);
+          cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
+          cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
         }
         const int live = min(kPagesPerTile, (L - j * kKv + kPage - 1) / kPage);
         int pid[kPagesPerTile];
@@ -425,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                          acc0 || kk > 0);
         tc::mma_commit(&bars[kBarODone + w]);
       };
-      cta_wait(&bars[kBarQ], 0, abort_flag, dev_error);
-      cta_wait(&bars[kBarKFull], 0, abort_flag, dev_error);
+      cta_wait(&bars[kBarQ], 0, abort_flag, dev_error, true);
+      cta_wait(&bars[kBarKFull], 0, abort_flag, dev_error, true);
       tc::fence_after_sync();
       issue_s(0, 0);
       issue_s(1, 0);
@@ -434,16 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       for (int j = 0; j < n_kv; ++j) {
         const int s = j & 1;
         const bool more = j + 1 < n_kv;
-        cta_wait(&bars[kBarPFull + 0], j & 1, abort_flag, dev_error);
-        cta_wait(&bars[kBarVFull + s], (j >> 1) & 1, abort_flag, dev_error);
+        cta_wait(&bars[kBarPFull + 0], j & 1, abort_flag, dev_error, true);
+        cta_wait(&bars[kBarVFull + s], (j >> 1) & 1, abort_flag, dev_error, true);
         tc::fence_after_sync();
         issue_pv(0, j);
         if (more) {
-          cta_wait(&bars[kBarKFull + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, dev_error);
+          cta_wait(&bars[kBarKFull + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, dev_error, true);
           tc::fence_after_sync();
           issue_s(0, j + 1);
         }
-        cta_wait(&bars[kBarPFull + 1], j & 1, abort_flag, dev_error);
+        cta_wait(&bars[kBarPFull + 1], j & 1, abort_flag, dev_error, true);
         tc::fence_after_sync();
         issue_pv(1, j);
         tc::mma_commit(&bars[kBarVEmpty + s]);
