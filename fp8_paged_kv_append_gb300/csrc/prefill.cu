@@ -79,6 +79,31 @@ enum {
   kNumBars = 19
 };
 
+// 2^x for a pair, on the FMA pipe (takes part of the exponentials off the
+// MUFU unit, which would otherwise bound the softmax).  Cody-Waite reduction
+// x = n + f with n = rint(x) via the 1.5*2^23 rounding constant and
+// f in [-1/2, 1/2]; 2^f by a degree-5 polynomial whose coefficients were
+// fitted here by least squares on Chebyshev nodes of [-1/2, 1/2] (max
+// relative error 2.2e-7 in fp32 Horner form); 2^n by adding n to the
+// exponent field.  Inputs below -127 give 0 (x is clamped there).
+__device__ __forceinline__ float2 exp2_poly(float2 x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  x.x = fmaxf(x.x, -127.f);
+  x.y = fmaxf(x.y, -127.f);
+  const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
+  const float2 r = __fadd2_rn(t, make_float2(-kRound, -kRound));  // rint(x)
+  const float2 f = __fadd2_rn(x, make_float2(-r.x, -r.y));
+  float2 p = make_float2(1.3266970636323094e-3f, 1.3266970636323094e-3f);
+  p = __ffma2_rn(p, f, make_float2(9.675459936261177e-3f, 9.675459936261177e-3f));
+  p = __ffma2_rn(p, f, make_float2(5.550742521882057e-2f, 5.550742521882057e-2f));
+  p = __ffma2_rn(p, f, make_float2(2.4022121727466583e-1f, 2.4022121727466583e-1f));
+  p = __ffma2_rn(p, f, make_float2(6.931469440460205e-1f, 6.931469440460205e-1f));
+  p = __ffma2_rn(p, f, make_float2(1.0000001192092896f, 1.0000001192092896f));
+  // t's low bits hold n (offset 0x4B400000, which vanishes after << 23)
+  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
+
 // Bounded wait shared by every role.  A wait that runs out sets the
 // CTA-wide abort flag (and the device error word); later waits return at
 // once, so every role runs to the end of its loop.
@@ -216,36 +241,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         }
       }
       // pass 2: p = 2^(s*scale - m) in pairs; fp32 row sum; P (fp16) over the
-      // already-read S columns: positions 64h.. land in P columns 32h..
+      // already-read S columns: positions 32c.. land in P columns 16c..
       const float2 sc2 = make_float2(qk_scale, qk_scale);
       const float2 nm2 = make_float2(-m_used, -m_used);
       float2 ps2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sr[2][32];
-        tc::tmem_ld32(tS + lane_base + h * 64, sr[0]);
-        tc::tmem_ld32(tS + lane_base + h * 64 + 32, sr[1]);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tc::tmem_ld32(tS + lane_base + c * 32, sr);
         tc::tmem_wait_ld();
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = h * 64 + c * 32 + 2 * e;
-            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * e]),
-                                                    __uint_as_float(sr[c][2 * e + 1])),
-                                        sc2, nm2);
-            float2 pp = make_float2(ex2(x.x), ex2(x.y));
-            if (need_mask) {
-              if (c0 > lim) pp.x = 0.f;
-              if (c0 + 1 > lim) pp.y = 0.f;
-            }
-            ps2 = __fadd2_rn(ps2, pp);
-            const __half2 hh = __floats2half2_rn(pp.x, pp.y);
-            pk[c * 16 + e] = *reinterpret_cast<const uint32_t *>(&hh);
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = c * 32 + 2 * e;
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sc2, nm2);
+          // 3 of every 8 pairs on the FMA pipe, the rest on MUFU
+          float2 pp = (e & 7) >= 5 ? exp2_poly(x) : make_float2(ex2(x.x), ex2(x.y));
+          if (need_mask) {
+            if (c0 > lim) pp.x = 0.f;
+            if (c0 + 1 > lim) pp.y = 0.f;
           }
+          ps2 = __fadd2_rn(ps2, pp);
+          const __half2 hh = __floats2half2_rn(pp.x, pp.y);
+          pk[e] = *reinterpret_cast<const uint32_t *>(&hh);
         }
-        tc::tmem_st32(tS + lane_base + h * 32, pk);
+        tc::tmem_st16(tS + lane_base + c * 16, pk);
       }
       tc::tmem_wait_st();
       l = l * alpha + (ps2.x + ps2.y);
@@ -337,50 +358,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         tc::tma_load_3d(sQ + w * kQBytes + kQBytes / 2, &tmap_q, 64, g * kGroup,
                         q0 + t_lo + w * kQTok, &bars[kBarQ]);
       }
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j & 1;
-        if (j >= 2) {
-          cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
-          cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
-        }
-        const int live = min(kPagesPerTile, (L - j * kKv + kPage - 1) / kPage);
-        int pid[kPagesPerTile];
-        uint32_t kbytes = 0;
-#pragma unroll
-        for (int i = 0; i < kPagesPerTile; ++i) {
-          pid[i] = -1;
-          if (i < live) {
-            const int pi = j * kPagesPerTile + i;
-            int p;
-            if (pi < kMaxIdPages) {
-              p = page_ids[pi];
-            } else {
-              p = __ldg(bt + pi);
-              if (p < 0 || p >= num_pages) {
-                flag_error(dev_error, K16V8_DEVERR_PAGE);
-                p = -1;
-              }
-            }
-            if (p >= 0) {
-              pid[i] = p;
-              kbytes += 2 * 2048;
-            }
+    }
+    // Per tile, lane i < 8 issues the three copies of page i; lane 0 first
+    // posts the tile's byte count on both barriers.
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j & 1;
+      if (j >= 2) {
+        cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
+        cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
+      }
+      const int live = min(kPagesPerTile, (L - j * kKv + kPage - 1) / kPage);
+      int pid = -1;
+      if (lane < live) {
+        const int pi = j * kPagesPerTile + lane;
+        if (pi < kMaxIdPages) {
+          pid = page_ids[pi];
+        } else {
+          pid = __ldg(bt + pi);
+          if (pid < 0 || pid >= num_pages) {
+            flag_error(dev_error, K16V8_DEVERR_PAGE);
+            pid = -1;
           }
         }
+      }
+      const uint32_t kbytes = __reduce_add_sync(0xffffffffu, pid >= 0 ? 2u * 2048u : 0u);
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bars[kBarKFull + s], kbytes);
         mbar_arrive_expect_tx(&bars[kBarVstFull + s], kbytes / 2);
+      }
+      __syncwarp();
+      if (pid >= 0) {
         uint8_t *k_dst = sK + s * kKStage;
         uint8_t *v_dst = sVst + s * kVstStage;
-#pragma unroll
-        for (int i = 0; i < kPagesPerTile; ++i) {
-          if (pid[i] < 0) continue;
-          const int row = (pid[i] * hkv + g) * kPage;
-          tc::tma_load_2d(k_dst + i * 2048, &tmap_k, 0, row, &bars[kBarKFull + s]);
-          tc::tma_load_2d(k_dst + kKBlk + i * 2048, &tmap_k, 64, row, &bars[kBarKFull + s]);
-          bulk_g2s(v_dst + i * 2048, v_cache + static_cast<int64_t>(row) * kHeadDim, 2048,
-                   &bars[kBarVstFull + s]);
-        }
+        const int row = (pid * hkv + g) * kPage;
+        tc::tma_load_2d(k_dst + lane * 2048, &tmap_k, 0, row, &bars[kBarKFull + s]);
+        tc::tma_load_2d(k_dst + kKBlk + lane * 2048, &tmap_k, 64, row, &bars[kBarKFull + s]);
+        bulk_g2s(v_dst + lane * 2048, v_cache + static_cast<int64_t>(row) * kHeadDim, 2048,
+                 &bars[kBarVstFull + s]);
       }
+    }
+    if (lane == 0) {
       // let the last copies land before shared memory is released (at once
       // on the normal path, where every copy has been consumed)
       for (int j = max(0, n_kv - 2); j < n_kv; ++j) {
