@@ -150,12 +150,17 @@ def kv_bytes(w) -> int:
 class DecodeBench:
     """Device state for timed decode steps over `replicas` copies of the pool."""
 
-    def __init__(self, w, device, split_chunk=512, replicas=None, fused=False):
+    def __init__(self, w, device, split_chunk=512, replicas=None, mode="chunked"):
+        """mode: "chunked" (append, split, merge), "fused" (append fused into
+        the split kernel, merge) or "balanced" (append, load-balanced split,
+        its merge)."""
         import torch
         from fp8_paged_kv_append_gb300 import k16v8 as K
+        assert mode in ("chunked", "fused", "balanced")
         self.K, self.torch, self.w, self.dev = K, torch, w, device
         self.chunk = split_chunk
-        self.fused = fused
+        self.mode = mode
+        self.fused = mode == "fused"
         pool_bytes = w.num_pages * w.num_kv_heads * 16 * w.head_dim * 3
         self.R = replicas or max(1, -(-4 * L2_BYTES // pool_bytes))
         P = w.num_pages
@@ -182,9 +187,14 @@ class DecodeBench:
         self.q = td(w.q)
         self.seq_lens = td(w.seq_lens)
         self.max_len = int(w.seq_lens.max())
-        self.ws = torch.empty(K.k16v8_decode_workspace_size(B, hq, d, self.max_len, self.chunk),
-                              dtype=torch.uint8, device=device)
-        self.po, self.pl = K.workspace_views(self.ws, B, hq, d, self.max_len, self.chunk)
+        if mode == "balanced":
+            self.ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d),
+                                  dtype=torch.uint8, device=device)
+        else:
+            self.ws = torch.empty(K.k16v8_decode_workspace_size(B, hq, d, self.max_len,
+                                                                self.chunk),
+                                  dtype=torch.uint8, device=device)
+            self.po, self.pl = K.workspace_views(self.ws, B, hq, d, self.max_len, self.chunk)
         self.out = torch.empty((B, hq, d), dtype=torch.float16, device=device)
         self.lse = torch.empty((B, hq), dtype=torch.float32, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -199,20 +209,37 @@ class DecodeBench:
                               self.vc, self.err)
         if ev:
             ev[1].record()
-        if self.fused:
+        self.split(i)
+        if ev:
+            ev[2].record()
+        self.merge()
+        if ev:
+            ev[3].record()
+
+    def split(self, i):
+        K, r = self.K, i % self.R
+        if self.mode == "fused":
             K.k16v8_paged_decode_append_split(self.q, self.k_new16, self.v_new16, self.kc, self.vc,
                                               self.v_scale, self.bt[r], self.seq_lens,
                                               self.max_len, self.w.sm_scale, self.chunk, self.ws,
                                               self.err)
+        elif self.mode == "balanced":
+            # block table and lengths are never written by the preceding kernel
+            K.k16v8_paged_decode_balanced_split(self.q, self.kc, self.vc, self.v_scale,
+                                                self.bt[r], self.seq_lens, self.w.sm_scale,
+                                                self.ws, self.out, self.lse, self.err,
+                                                flags=K.DECODE_METADATA_READY)
         else:
             K.k16v8_paged_decode_split(self.q, self.kc, self.vc, self.v_scale, self.bt[r],
                                        self.seq_lens, self.max_len, self.w.sm_scale, self.chunk,
                                        self.ws, self.err)
-        if ev:
-            ev[2].record()
-        K.k16v8_merge_states(self.po, self.pl, self.seq_lens, self.chunk, self.out, self.lse)
-        if ev:
-            ev[3].record()
+
+    def merge(self):
+        K = self.K
+        if self.mode == "balanced":
+            K.k16v8_merge_balanced(self.ws, self.w.num_kv_heads, self.out, self.lse)
+        else:
+            K.k16v8_merge_states(self.po, self.pl, self.seq_lens, self.chunk, self.out, self.lse)
 
     def capture(self, steps, with_events=False):
         """One CUDA graph per step, so the timed region replays pre-built
@@ -231,25 +258,29 @@ class DecodeBench:
         return graphs, evs
 
     def run(self, steps, warmup):
-        """Time `steps` replays of per-step graphs (no timing nodes inside, so
-        programmatic launch edges between the kernels stay intact), then the
+        """Time `steps` decode steps captured back to back into one CUDA graph
+        (no timing nodes inside, so the programmatic launch edges between all
+        the kernels stay intact, as in a whole-model decode graph), then the
         average duration of each kernel from a graph of `steps` launches of
         that kernel alone over the same state."""
         torch = self.torch
         for i in range(warmup):  # eager warm-up also configures kernel attributes
             self.step(i)
         torch.cuda.synchronize(self.dev)
-        graphs, _ = self.capture(steps, with_events=False)
-        for i in range(warmup):
-            graphs[i % steps].replay()
+        side = torch.cuda.Stream(self.dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
+            for i in range(steps):
+                self.step(i)
+        for _ in range(-(-warmup // steps)):
+            graph.replay()
         torch.cuda.synchronize(self.dev)
         barrier()
         torch.cuda.synchronize(self.dev)
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
-        for g in graphs:
-            g.replay()
+        graph.replay()
         t1.record()
         torch.cuda.synchronize(self.dev)
         barrier()
@@ -264,21 +295,12 @@ class DecodeBench:
         `steps` launches (rotating over the pool replicas), timed as a block."""
         torch, K = self.torch, self.K
         outs = []
-        split = (lambda i: K.k16v8_paged_decode_append_split(
-                     self.q, self.k_new16, self.v_new16, self.kc, self.vc, self.v_scale,
-                     self.bt[i % self.R], self.seq_lens, self.max_len, self.w.sm_scale,
-                     self.chunk, self.ws, self.err)) if self.fused else (
-                 lambda i: K.k16v8_paged_decode_split(self.q, self.kc, self.vc, self.v_scale,
-                                                      self.bt[i % self.R], self.seq_lens,
-                                                      self.max_len, self.w.sm_scale, self.chunk,
-                                                      self.ws, self.err))
         kinds = [
             (lambda i: None) if self.fused else (
                 lambda i: K.k16v8_kv_append(self.k_new, self.v_new, self.slots_new[i % self.R],
                                             self.v_scale, self.kc, self.vc, self.err)),
-            split,
-            lambda i: K.k16v8_merge_states(self.po, self.pl, self.seq_lens, self.chunk,
-                                           self.out, self.lse)]
+            self.split,
+            lambda i: self.merge()]
         side = torch.cuda.Stream(self.dev)
         for ki, fn in enumerate(kinds):
             if ki == 0 and self.fused:
@@ -324,9 +346,15 @@ class DecodeBench:
             d_slots.copy_(h_slots[r], non_blocking=True)
             K.k16v8_kv_append(d_in["k_new"], d_in["v_new"], d_slots, self.v_scale, self.kc,
                               self.vc, self.err)
-            K.k16v8_paged_decode_attention(d_in["q"], self.kc, self.vc, self.v_scale, d_bt,
-                                           d_in["seq_lens"], self.max_len, w.sm_scale,
-                                           self.chunk, self.ws, self.out, self.lse, self.err)
+            if self.mode == "balanced":
+                K.k16v8_paged_decode_attention_balanced(d_in["q"], self.kc, self.vc,
+                                                        self.v_scale, d_bt, d_in["seq_lens"],
+                                                        w.sm_scale, self.ws, self.out, self.lse,
+                                                        self.err, flags=K.DECODE_METADATA_READY)
+            else:
+                K.k16v8_paged_decode_attention(d_in["q"], self.kc, self.vc, self.v_scale, d_bt,
+                                               d_in["seq_lens"], self.max_len, w.sm_scale,
+                                               self.chunk, self.ws, self.out, self.lse, self.err)
             h_out.copy_(self.out, non_blocking=True)
             h_lse.copy_(self.lse, non_blocking=True)
 
@@ -641,6 +669,8 @@ def main():
                     help="skip the secondary 8K/b16 line inside the JSON")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--decode", default="chunked", choices=["chunked", "balanced"],
+                    help="decode schedule of the main line")
     ap.add_argument("--split-chunk", type=int, default=0,
                     help="tokens per split-KV chunk of the main workload (0: its default)")
     args = ap.parse_args()
@@ -673,7 +703,7 @@ def main():
     w, label, chunk = make_workload(args.workload)
     if args.split_chunk:
         chunk = args.split_chunk
-    bench = DecodeBench(w, device, split_chunk=chunk)
+    bench = DecodeBench(w, device, split_chunk=chunk, mode=args.decode)
     clocks = ClockSampler(local_rank).start()
     ms, seg = bench.run(args.steps, max(args.warmup, 3))
     clk = clocks.stop()
@@ -737,7 +767,7 @@ def main():
         for name, (wf, _, cf) in (("decode_1k_b32", make_workload("1k")),
                                   ("decode_8k_b16", make_workload("8k"))):
             torch.cuda.empty_cache()
-            bf = DecodeBench(wf, device, split_chunk=cf, fused=True)
+            bf = DecodeBench(wf, device, split_chunk=cf, mode="fused")
             msf, segf = bf.run(max(10, args.steps // 2), 3)
             sf = float(np.mean(segf[:, 1])) * 1e3
             line["extra"][f"{name}_fused_append"] = {

@@ -14,85 +14,21 @@
 //    bulk-async copies per page -- the 4 KB K tile and the 2 KB V tile of one
 //    (page, KV head) are contiguous in the cache layout -- completing on an
 //    mbarrier; no register staging, no address arithmetic per element.
-//  * Q.K: eight lanes own one token (16 dims each, conflict-free 16-byte
-//    shared loads), fp16-operand FMAs with fp32 accumulation against the
-//    query held as packed fp16 pairs, then a 3-step reduce-scatter so each
-//    lane ends with one (token, head) score: 4 shuffles per 4 tokens.
-//  * Online softmax in the log2 domain per page (running max / sum).
-//  * P.V: each lane owns 4 dims of every token; E4M3 -> fp16 pairs by the
-//    hardware cvt, fp16x2 FMAs summed over one 16-token page (p <= 1 and
-//    |v| <= 448 keep a page sum below 7168), folded into fp32 state per
-//    page.  The per-head value scale is applied once to the final partial
-//    (it factors out of the sum).
+//  * Per page: Q.K, online softmax and P.V as in decode_page.cuh; the
+//    per-head value scale is applied once to the final partial.
 //  * The four warps' states are combined in shared memory; the CTA writes
 //    one fp32 partial row per query head plus its natural-log LSE.
 //  * Launched with programmatic stream serialization: griddepcontrol.wait
 //    precedes every read of inputs.
-#include <math.h>
-
-#include "k16v8_device.cuh"
+#include "decode_page.cuh"
 
 namespace k16v8 {
-
-constexpr int kWarps = 4;
-constexpr int kStages = 2;
-constexpr int kMinBlocks = 4;
-constexpr int kKPageBytes = kPage * kHeadDim * 2;  // 4096
-constexpr int kVPageBytes = kPage * kHeadDim;      // 2048
-constexpr unsigned kFull = 0xffffffffu;
-
-template <int kVBytes>
-struct __align__(128) WarpRingT {
-  uint8_t k[kStages][kKPageBytes];
-  uint8_t v[kStages][kVBytes];
-  uint32_t p[kPage * kGroup];  // p[token][head] as a duplicated fp16 pair (p, p)
-  float alpha[kGroup];         // rescale factor of the running state
-  uint64_t bar[kStages];
-};
-using WarpRing = WarpRingT<kVPageBytes>;             // E4M3 values
-using WarpRing16 = WarpRingT<2 * kVPageBytes>;       // FP16 values (the FP16-KV control)
 
 __host__ __device__ constexpr size_t ids_bytes(int split_chunk) {
   return ((static_cast<size_t>(split_chunk / kPage) * sizeof(int) + 15) / 16) * 16;
 }
 static size_t decode_smem_bytes(int split_chunk, bool vf16) {
   return kWarps * (vf16 ? sizeof(WarpRing16) : sizeof(WarpRing)) + ids_bytes(split_chunk);
-}
-
-// acc += a.lo * b.lo + a.hi * b.hi with fp16 operands, fp32 accumulation
-// (each product is exact in fp32; one rounding per FMA).
-__device__ __forceinline__ float fma_h2(uint32_t a, uint32_t b, float acc) {
-  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
-      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
-      "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(a), "r"(b));
-  return acc;
-}
-
-__device__ __forceinline__ uint32_t e4m3x2_to_h2bits(uint16_t v) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-  return r;
-}
-
-// Sum acc[0..3] over the 8 lanes of a token group; lane j of the group ends
-// with the total of head j >> 1.
-__device__ __forceinline__ float reduce_scatter8(const float (&acc)[kGroup], int j) {
-  const bool up4 = j & 4;
-  const float s0 = up4 ? acc[0] : acc[2];
-  const float s1 = up4 ? acc[1] : acc[3];
-  float k0 = up4 ? acc[2] : acc[0];
-  float k1 = up4 ? acc[3] : acc[1];
-  k0 += __shfl_xor_sync(kFull, s0, 4);
-  k1 += __shfl_xor_sync(kFull, s1, 4);
-  const bool up2 = j & 2;
-  const float snd = up2 ? k0 : k1;
-  float kp = up2 ? k1 : k0;
-  kp += __shfl_xor_sync(kFull, snd, 2);
-  kp += __shfl_xor_sync(kFull, kp, 1);
-  return kp;
 }
 
 // kAppend: also write each sequence's new token (k_new / v_new, position
@@ -171,35 +107,14 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
   if (lane == 0)
     for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
 
-  // Query of the group's 4 heads as packed fp16 pairs.  Lane j of a token
-  // group owns dims [8j, 8j+8) and [64+8j, 64+8j+8): qh[h][0..3], qh[h][4..7].
   const int j = lane & 7;
   uint32_t qh[kGroup][8];
-  {
-    const __half *qb = q + (static_cast<int64_t>(b) * hq + g * kGroup) * kHeadDim;
-#pragma unroll
-    for (int h = 0; h < kGroup; ++h) {
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint4 raw =
-            __ldg(reinterpret_cast<const uint4 *>(qb + h * kHeadDim + part * 64 + j * 8));
-        qh[h][part * 4 + 0] = raw.x;
-        qh[h][part * 4 + 1] = raw.y;
-        qh[h][part * 4 + 2] = raw.z;
-        qh[h][part * 4 + 3] = raw.w;
-      }
-    }
-  }
+  load_group_query(q + (static_cast<int64_t>(b) * hq + g * kGroup) * kHeadDim, j, qh);
   const float qs = sm_scale * kLog2e;  // scores in the log2 domain
 
   const int hsel = j >> 1;  // head whose score this lane holds
-  float m_run = -INFINITY, l_run = 0.f;
-  // P.V state: this lane's dims [4*lane, 4*lane+4) of the 4 heads, fp32
-  // across pages; within a page the products accumulate as fp16 pairs
-  // (p <= 1 and |v| <= 448, so a 16-token page sum stays below 7168).
-  float2 o[kGroup][2];
-#pragma unroll
-  for (int h = 0; h < kGroup; ++h) o[h][0] = o[h][1] = make_float2(0.f, 0.f);
+  WarpState st;
+  st.reset();
 
   int k = 0;
   bool ok = true;
@@ -240,92 +155,7 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
       }
       __syncwarp();
     }
-    if (page_ids[i] >= 0) {
-      // ---- scores of 16 tokens x 4 heads ----
-      const uint8_t *kp = ring.k[s];
-      float sc[4];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int t = it * 4 + (lane >> 3);
-        const uint4 a = *reinterpret_cast<const uint4 *>(kp + t * 256 + j * 16);
-        const uint4 bq = *reinterpret_cast<const uint4 *>(kp + t * 256 + 128 + j * 16);
-        float acc[kGroup], acc2[kGroup];
-#pragma unroll
-        for (int h = 0; h < kGroup; ++h) {
-          acc[h] = fma_h2(qh[h][0], a.x, 0.f);
-          acc2[h] = fma_h2(qh[h][4], bq.x, 0.f);
-          acc[h] = fma_h2(qh[h][1], a.y, acc[h]);
-          acc2[h] = fma_h2(qh[h][5], bq.y, acc2[h]);
-          acc[h] = fma_h2(qh[h][2], a.z, acc[h]);
-          acc2[h] = fma_h2(qh[h][6], bq.z, acc2[h]);
-          acc[h] = fma_h2(qh[h][3], a.w, acc[h]);
-          acc2[h] = fma_h2(qh[h][7], bq.w, acc2[h]);
-          acc[h] += acc2[h];
-        }
-        const float v = reduce_scatter8(acc, j) * qs;
-        sc[it] = t < valid ? v : -INFINITY;
-      }
-      // ---- online softmax (log2 domain) ----
-      float pm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-      pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 8));
-      pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 16));
-      const float m_new = fmaxf(m_run, pm);
-      const float alpha = ex2(m_run - m_new);
-      float p[4];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) p[it] = ex2(sc[it] - m_new);
-      l_run = l_run * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
-      m_run = m_new;
-      if ((lane & 1) == 0) {
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const uint32_t ph = __half_as_ushort(__float2half_rn(p[it]));
-          ring.p[(it * 4 + (lane >> 3)) * kGroup + hsel] = ph | (ph << 16);
-        }
-        if (lane < 8) ring.alpha[hsel] = alpha;
-      }
-      __syncwarp();
-      // ---- P.V over this page: lane owns 4 dims of every token ----
-      __half2 acc[kGroup][2];
-#pragma unroll
-      for (int h = 0; h < kGroup; ++h) acc[h][0] = acc[h][1] = __float2half2_rn(0.f);
-      const uint8_t *vp = ring.v[s] + lane * (kVF16 ? 8 : 4);
-      auto pv_token = [&](int t) {
-        __half2 v01, v23;
-        if constexpr (kVF16) {
-          const uint2 raw = *reinterpret_cast<const uint2 *>(vp + t * kHeadDim * 2);
-          v01 = *reinterpret_cast<const __half2 *>(&raw.x);
-          v23 = *reinterpret_cast<const __half2 *>(&raw.y);
-        } else {
-          const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp + t * kHeadDim);
-          v01 = e4m3x2_to_half2(static_cast<uint16_t>(raw & 0xffffu));
-          v23 = e4m3x2_to_half2(static_cast<uint16_t>(raw >> 16));
-        }
-        const uint4 pp = *reinterpret_cast<const uint4 *>(ring.p + t * kGroup);
-        const uint32_t pw[kGroup] = {pp.x, pp.y, pp.z, pp.w};
-#pragma unroll
-        for (int h = 0; h < kGroup; ++h) {
-          const __half2 ph = *reinterpret_cast<const __half2 *>(&pw[h]);
-          acc[h][0] = __hfma2(ph, v01, acc[h][0]);
-          acc[h][1] = __hfma2(ph, v23, acc[h][1]);
-        }
-      };
-      if (valid == kPage) {
-#pragma unroll
-        for (int t = 0; t < kPage; ++t) pv_token(t);
-      } else {
-        for (int t = 0; t < valid; ++t) pv_token(t);
-      }
-      // fold the page into the fp32 state: o = o * alpha + page sum
-      const float4 al = *reinterpret_cast<const float4 *>(ring.alpha);
-      const float alv[kGroup] = {al.x, al.y, al.z, al.w};
-#pragma unroll
-      for (int h = 0; h < kGroup; ++h) {
-        const float2 a2 = make_float2(alv[h], alv[h]);
-        o[h][0] = __ffma2_rn(o[h][0], a2, __half22float2(acc[h][0]));
-        o[h][1] = __ffma2_rn(o[h][1], a2, __half22float2(acc[h][1]));
-      }
-    }
+    if (page_ids[i] >= 0) attend_page<kVF16>(ring, s, valid, qh, qs, st);
     __syncwarp();
     if (lane == 0 && k + kStages < n_my) {
       fence_proxy_async();
@@ -346,6 +176,7 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
   pdl_launch_dependents();
 
   // ---- sum each head's l over its lanes (lanes j, j^1 hold copies) ----
+  float l_run = st.l;
   l_run += __shfl_xor_sync(kFull, l_run, 8);
   l_run += __shfl_xor_sync(kFull, l_run, 16);
 
@@ -355,13 +186,13 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
   float *wm = wo + kWarps * kGroup * kHeadDim;        // [warp][head]
   float *wl = wm + kWarps * kGroup;
   if (lane < 8 && (lane & 1) == 0) {
-    wm[warp * kGroup + hsel] = m_run;
+    wm[warp * kGroup + hsel] = st.m;
     wl[warp * kGroup + hsel] = l_run;
   }
 #pragma unroll
   for (int h = 0; h < kGroup; ++h)
     *reinterpret_cast<float4 *>(wo + (warp * kGroup + h) * kHeadDim + lane * 4) =
-        make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+        make_float4(st.o[h][0].x, st.o[h][0].y, st.o[h][1].x, st.o[h][1].y);
   __syncthreads();
   {
     const int h = threadIdx.x >> 5;

@@ -26,6 +26,7 @@ K16V8_ERR_STATIC_SCRATCH_LIMIT = 6
 STATIC_SCRATCH_BYTES = 32 << 20
 K16V8_F16 = 0
 K16V8_F32 = 1
+DECODE_METADATA_READY = 1
 DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8, 16
 PAGE_SIZE = 16
 HEAD_DIM = 128
@@ -65,6 +66,14 @@ SIGNATURES = {
     "k16v8_paged_prefill_attention": (_i32, [_P, _P, _i32, _i32, _P, _P, _P, _P, _i32, _P,
                                              _i32, _i32, _i32, _i32, _i32, _f32, _P, _P, _P,
                                              _P]),
+    "k16v8_decode_balanced_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "k16v8_paged_decode_attention_balanced": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32,
+                                                     _i32, _i32, _i32, _f32, _P, _sz, _P, _P,
+                                                     _i32, _P, _P]),
+    "k16v8_paged_decode_balanced_split": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32,
+                                                 _i32, _i32, _i32, _f32, _P, _sz, _P, _P, _i32,
+                                                 _P, _P]),
+    "k16v8_merge_balanced": (_i32, [_P, _sz, _i32, _i32, _i32, _i32, _P, _P, _P]),
     "k16v8_read_device_error": (_i32, [_P, _P, ctypes.POINTER(_i32)]),
     "k16v8_status_string": (ctypes.c_char_p, [_i32]),
 }
@@ -289,6 +298,45 @@ def k16v8_paged_decode_attention_static(q, k_cache, v_cache, v_scale, block_tabl
         k_cache.shape[0], float(sm_scale), int(split_chunk), _ptr(out), _ptr(lse),
         _ptr(dev_error), _stream(stream))
     _check("k16v8_paged_decode_attention_static", st)
+
+
+def k16v8_decode_balanced_workspace_size(batch, num_qo_heads, head_dim) -> int:
+    """Bytes of workspace k16v8_paged_decode_attention_balanced needs on the
+    current device (0 for an unsupported shape)."""
+    return int(load_library().k16v8_decode_balanced_workspace_size(batch, num_qo_heads, head_dim))
+
+
+def k16v8_paged_decode_attention_balanced(q, k_cache, v_cache, v_scale, block_table, seq_lens,
+                                          sm_scale, workspace, out, lse=None, dev_error=None,
+                                          stream=None, flags=0):
+    """Decode attention with every CTA given the same number of KV tiles."""
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_attention_balanced(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, hq, k_cache.shape[1], d, k_cache.shape[0],
+        float(sm_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), _ptr(lse), int(flags), _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_decode_attention_balanced", st)
+
+
+def k16v8_paged_decode_balanced_split(q, k_cache, v_cache, v_scale, block_table, seq_lens,
+                                      sm_scale, workspace, out, lse=None, dev_error=None,
+                                      stream=None, flags=0):
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_balanced_split(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, hq, k_cache.shape[1], d, k_cache.shape[0],
+        float(sm_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), _ptr(lse), int(flags), _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_decode_balanced_split", st)
+
+
+def k16v8_merge_balanced(workspace, num_kv_heads, out, lse=None, stream=None):
+    B, hq, d = out.shape
+    st = load_library().k16v8_merge_balanced(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), B, hq, int(num_kv_heads),
+        d, _ptr(out), _ptr(lse), _stream(stream))
+    _check("k16v8_merge_balanced", st)
 
 
 def k16v8_read_device_error(dev_error, stream=None) -> int:

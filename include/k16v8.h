@@ -191,6 +191,65 @@ int32_t k16v8_paged_decode_attention(const void *q, const void *k_cache,
                                      int32_t *dev_error, void *stream);
 
 /*
+ * paged_decode_attention_balanced -- the same result as
+ * k16v8_paged_decode_attention (split-KV attention, then the log-sum-exp
+ * merge, "Matched diagnostic profiles"), with the split chosen by the device
+ * instead of a fixed split_chunk: all (sequence, KV head, page) tiles are
+ * cut into one full wave of equal CTA ranges (SMs x 4 CTAs), so ragged
+ * batches leave no tail wave.  Two launches (attention, merge) on `stream`.
+ *
+ *   batch        0 .. 8192 (0: nothing is launched)
+ *   workspace    device, 256-B aligned, at least
+ *                k16v8_decode_balanced_workspace_size(batch, num_qo_heads,
+ *                head_dim) bytes, sized for the CURRENT device's SM count;
+ *                contents need no initialisation and are overwritten
+ *   seq_lens     device int32 [batch]; no max_seq_len is needed
+ *   flags        0, or K16V8_DECODE_METADATA_READY: the caller guarantees
+ *                that block_table and seq_lens are not written by the kernel
+ *                launched immediately before this call on `stream` (host
+ *                copies and earlier kernels are fine).  The attention kernel
+ *                then reads them, and plans its work, before it waits for
+ *                that kernel to finish (programmatic dependent launch); the
+ *                cache, q, the workspace and the outputs are still touched
+ *                only after the wait.  Without the flag nothing is read
+ *                before the wait.
+ * Other arguments, outputs and device errors as for
+ * k16v8_paged_decode_attention.  batch * max_pages_per_seq * num_kv_heads
+ * and num_pages * num_kv_heads must stay below 2^31
+ * (K16V8_ERR_INVALID_ARG otherwise).
+ */
+#define K16V8_DECODE_METADATA_READY 0x1
+
+size_t k16v8_decode_balanced_workspace_size(int32_t batch, int32_t num_qo_heads,
+                                            int32_t head_dim);
+
+/*
+ * The two launches of paged_decode_attention_balanced, for callers that
+ * schedule them separately (same arguments; the workspace carries the work
+ * plan and the partials from the first to the second).
+ * paged_decode_balanced_split already writes the rows of every (sequence,
+ * KV head) segment that one CTA held whole; merge_balanced writes the rest
+ * (cut segments, and empty sequences: zeros and LSE -inf).
+ */
+int32_t k16v8_paged_decode_balanced_split(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
+    float *lse, int32_t flags, int32_t *dev_error, void *stream);
+
+int32_t k16v8_merge_balanced(const void *workspace, size_t workspace_bytes, int32_t batch,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                             void *out, float *lse, void *stream);
+
+int32_t k16v8_paged_decode_attention_balanced(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
+    float *lse, int32_t flags, int32_t *dev_error, void *stream);
+
+/*
  * paged_decode_append_split / paged_decode_append_attention -- one decode
  * step's cache write fused into the attention kernel: equivalent to
  * k16v8_kv_append of each sequence's new token at position seq_lens[b] - 1
