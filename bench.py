@@ -126,10 +126,27 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def traffic_from_profiles(kernel_src: str):
-    """DRAM bytes per launch of the decode split kernel from the committed ncu
-    summary, or None when the kernel source changed since that capture."""
-    path = os.path.join(ROOT, "profiles", "decode_split_1k_b32.md")
+KERNEL_SOURCES = {
+    "chunked": ("decode_split_1k_b32.md", ["decode.cu", "decode_page.cuh", "k16v8_device.cuh"]),
+    "balanced": ("decode_balanced_1k_b32.md",
+                 ["decode_balanced.cu", "decode_page.cuh", "k16v8_device.cuh"]),
+}
+
+
+def sources_sha256(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "fp8_paged_kv_append_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_from_profiles(mode: str):
+    """DRAM bytes per launch of the decode attention kernel of `mode` from the
+    committed ncu summary, or None when its sources changed since that
+    capture."""
+    prof, srcs = KERNEL_SOURCES[mode]
+    path = os.path.join(ROOT, "profiles", prof)
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -137,14 +154,19 @@ def traffic_from_profiles(kernel_src: str):
     m_tr = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
     if not m_src or not m_tr:
         return None
-    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return float(m_tr.group(1)) if cur == m_src.group(1) else None
+    return float(m_tr.group(1)) if sources_sha256(srcs) == m_src.group(1) else None
 
 
 # ---- the decode workload on the GPU ---------------------------------------------
 
 def kv_bytes(w) -> int:
     return int(w.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 3
+
+
+def replicas_for(w) -> int:
+    """Pool copies rotated between steps so that every step reads HBM (>= 4x L2)."""
+    pool_bytes = w.num_pages * w.num_kv_heads * 16 * w.head_dim * 3
+    return max(1, -(-4 * L2_BYTES // pool_bytes))
 
 
 class DecodeBench:
@@ -161,8 +183,7 @@ class DecodeBench:
         self.chunk = split_chunk
         self.mode = mode
         self.fused = mode == "fused"
-        pool_bytes = w.num_pages * w.num_kv_heads * 16 * w.head_dim * 3
-        self.R = replicas or max(1, -(-4 * L2_BYTES // pool_bytes))
+        self.R = replicas or replicas_for(w)
         P = w.num_pages
         self.P = P
         B, hq, d = w.q.shape
@@ -547,7 +568,7 @@ def prefill_line(p, device, steps, warmup, tensor_peak):
 
 # ---- full-pool ragged decode across 40 layers ------------------------------------
 
-def fullpool_line(device, steps, warmup, hbm_peak, layers=40):
+def fullpool_line(device, steps, warmup, hbm_peak, layers=40, schedule="chunked"):
     """One decode step through all layers' attention (per layer: append the new
     token, split-KV attention, merge) over 32 GiB of pools, replayed as one
     CUDA graph."""
@@ -570,7 +591,7 @@ def fullpool_line(device, steps, warmup, hbm_peak, layers=40):
     td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
     step = MultiLayerDecode([p[0] for p in pools], [p[1] for p in pools], [p[2] for p in pools],
                             td(lay.block_table), td(lay.seq_lens), td(slots), int(L.max()), 40,
-                            split_chunk=512)
+                            split_chunk=512, schedule=schedule)
     outs = [torch.empty((B, 40, 128), dtype=torch.float16, device=device) for _ in range(layers)]
     lses = [torch.empty((B, 40), dtype=torch.float32, device=device) for _ in range(layers)]
     step.capture(qs, kn, vn, outs, lses)
@@ -592,7 +613,9 @@ def fullpool_line(device, steps, warmup, hbm_peak, layers=40):
     torch.cuda.empty_cache()
     return {"workload": f"full pool: {layers} layers x {P} pages (223,696 slots, 32 GiB), batch "
                         f"{B}, seq_lens {int(L.min())}..{int(L.max())} (sum {int(L.sum())}, "
-                        f"{lay.draws} draw(s)), split 512, one CUDA graph per step",
+                        f"{lay.draws} draw(s)), "
+                        + ("split 512" if schedule == "chunked" else "load-balanced split")
+                        + ", one CUDA graph per step",
             "ms_per_step": round(ms, 4), "us_per_layer_step": round(ms * 1e3 / layers, 2),
             "kv_bytes_per_step": kvb, "value": round(kvb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
@@ -650,12 +673,47 @@ def make_workload(name):
     raise SystemExit(f"unknown workload {name}")
 
 
-def config_of(w, label, chunk, replicas):
+def config_of(w, label, chunk, replicas, mode="balanced"):
+    sched = ("load-balanced split: one full wave (SMs x 4 CTAs) of equal (sequence, KV head, "
+             "page) tile ranges, LSE merge of cut segments") if mode == "balanced" else \
+        f"split-KV chunks of {chunk} tokens, LSE merge"
     return {"workload": f"Phi-4-shaped {label}: one layer, 40 q / 10 KV heads, head_dim 128, "
                         "16-token pages, FP16 K + E4M3 V",
             "batch": int(w.batch), "seq_lens": f"{int(w.seq_lens.min())}..{int(w.seq_lens.max())}",
-            "cached_tokens": int(w.seq_lens.sum()), "split_chunk": chunk,
+            "cached_tokens": int(w.seq_lens.sum()), "schedule": sched,
             "l2": f"{replicas} rotating pool replicas (>= 4x L2) so every step reads HBM"}
+
+
+KERNEL_NAMES = {
+    "chunked": ("decode_split", "merge_states", "decode_split_kernel"),
+    "balanced": ("decode_balanced", "merge_balanced", "decode_balanced_kernel"),
+    "fused": ("decode_append_split", "merge_states", "decode_split_kernel<append>"),
+}
+
+
+def decode_line(w, label, chunk, mode, device, steps, hbm_peak):
+    """Secondary decode line: one workload, one schedule."""
+    import torch
+    b = DecodeBench(w, device, split_chunk=chunk, mode=mode)
+    ms, seg = b.run(steps, 3)
+    split_name, merge_name, _ = KERNEL_NAMES[mode]
+    kvb = kv_bytes(w)
+    s_us = float(np.mean(seg[:, 1])) * 1e3
+    sb = kvb + w.batch * w.num_qo_heads * w.head_dim * 2
+    out = {"value": round(kvb / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "us_per_layer_step": round(ms * 1e3, 2),
+           "kernel_us": {"kv_append": round(float(np.mean(seg[:, 0])) * 1e3, 2),
+                         split_name: round(s_us, 2),
+                         merge_name: round(float(np.mean(seg[:, 2])) * 1e3, 2)},
+           "split_frac_of_hbm_peak": round(sb / (s_us * 1e-6) / 1e9 / hbm_peak, 4),
+           "step_frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+           "config": config_of(w, label, chunk, b.R, mode)}
+    if mode == "fused":
+        del out["kernel_us"]["kv_append"]
+        out["step"] = "append fused into the split kernel, then merge (2 launches)"
+    del b
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -669,7 +727,7 @@ def main():
                     help="skip the secondary 8K/b16 line inside the JSON")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--decode", default="chunked", choices=["chunked", "balanced"],
+    ap.add_argument("--decode", default="balanced", choices=["chunked", "balanced"],
                     help="decode schedule of the main line")
     ap.add_argument("--split-chunk", type=int, default=0,
                     help="tokens per split-KV chunk of the main workload (0: its default)")
@@ -686,7 +744,8 @@ def main():
         torch.cuda.set_device(0)
         K.load_library()
         print(json.dumps({"fullpool_40_layers": fullpool_line(
-            torch.device("cuda", 0), args.steps, max(3, args.warmup), load_peaks()[0])}))
+            torch.device("cuda", 0), args.steps, max(3, args.warmup), load_peaks()[0],
+            schedule=args.decode)}))
         return
 
     import torch
@@ -717,24 +776,22 @@ def main():
     split_us = float(np.mean(seg[:, 1])) * 1e3
     split_bytes = kvb + B * hq * d * 2
     achieved = split_bytes / (split_us * 1e-6) / 1e9
-    traffic = traffic_from_profiles(os.path.join(ROOT, "fp8_paged_kv_append_gb300", "csrc",
-                                                 "decode.cu"))
-    if traffic is not None and args.workload != "1k":
-        traffic = None
+    traffic = traffic_from_profiles(args.decode) if args.workload == "1k" else None
+    split_name, merge_name, kernel_name = KERNEL_NAMES[args.decode]
     line = {
         "metric": METRIC, "value": round(units / (t_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(t_ms, 5), "us_per_layer_step": round(t_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,1) Q/K/V, E4M3 V with per-head amax/448 scales)",
-        "config": config_of(w, label, chunk, bench.R),
+        "config": config_of(w, label, chunk, bench.R, args.decode),
         "kernel_us": {"kv_append": round(float(np.mean(seg[:, 0])) * 1e3, 2),
-                      "decode_split": round(split_us, 2),
-                      "merge_states": round(float(np.mean(seg[:, 2])) * 1e3, 2)},
+                      split_name: round(split_us, 2),
+                      merge_name: round(float(np.mean(seg[:, 2])) * 1e3, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "traffic": traffic, "peak_kind": f"{peak_kind} (copy bandwidth)",
-                     "kernel": "decode_split_kernel",
+                     "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": split_bytes},
         "e2e": {"value": round(units / (te_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(te_ms, 4), "h2d_bytes_per_step": h2d,
@@ -745,48 +802,38 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = run_cpu_baseline(w, chunk, args.cpu_budget)
     if not args.no_extra and args.workload == "1k":
-        w8, label8, chunk8 = make_workload("8k")
+        from fp8_paged_kv_append_gb300 import workloads
         del bench
         torch.cuda.empty_cache()
-        b8 = DecodeBench(w8, device, split_chunk=chunk8)
-        ms8, seg8 = b8.run(max(10, args.steps // 2), 3)
-        t8, u8 = aggregate(ms8, kv_bytes(w8))
-        s8 = float(np.mean(seg8[:, 1])) * 1e3
-        sb8 = kv_bytes(w8) + w8.batch * w8.num_qo_heads * w8.head_dim * 2
-        line["extra"] = {"decode_8k_b16": {
-            "value": round(u8 / (t8 * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "us_per_layer_step": round(t8 * 1e3, 2),
-            "kernel_us": {"kv_append": round(float(np.mean(seg8[:, 0])) * 1e3, 2),
-                          "decode_split": round(s8, 2),
-                          "merge_states": round(float(np.mean(seg8[:, 2])) * 1e3, 2)},
-            "split_frac_of_hbm_peak": round(sb8 / (s8 * 1e-6) / 1e9 / hbm_peak, 4),
-            "step_frac_of_hbm_peak": round(u8 / (t8 * 1e-3) / 1e9 / hbm_peak, 4),
-            "config": config_of(w8, label8, chunk8, b8.R)}}
-    if not args.no_extra and args.workload == "1k":
-        from fp8_paged_kv_append_gb300 import workloads
-        for name, (wf, _, cf) in (("decode_1k_b32", make_workload("1k")),
-                                  ("decode_8k_b16", make_workload("8k"))):
+        other = "chunked" if args.decode == "balanced" else "balanced"
+        n2 = max(10, args.steps // 2)
+        w8, label8, chunk8 = make_workload("8k")
+        line["extra"] = {
+            "decode_8k_b16": decode_line(w8, label8, chunk8, args.decode, device, n2, hbm_peak),
+            f"decode_1k_b32_{other}": decode_line(w, label, chunk, other, device, n2, hbm_peak),
+            f"decode_8k_b16_{other}": decode_line(w8, label8, chunk8, other, device, n2,
+                                                  hbm_peak)}
+        for name, (wf, lf, cf) in (("decode_1k_b32", (w, label, chunk)),
+                                   ("decode_8k_b16", (w8, label8, chunk8))):
+            line["extra"][f"{name}_fused_append"] = decode_line(wf, lf, cf, "fused", device, n2,
+                                                                hbm_peak)
+        for name, (wf, _, cf) in (("decode_1k_b32", (w, label, chunk)),
+                                  ("decode_8k_b16", (w8, label8, chunk8))):
             torch.cuda.empty_cache()
-            bf = DecodeBench(wf, device, split_chunk=cf, mode="fused")
-            msf, segf = bf.run(max(10, args.steps // 2), 3)
-            sf = float(np.mean(segf[:, 1])) * 1e3
-            line["extra"][f"{name}_fused_append"] = {
-                "us_per_layer_step": round(msf * 1e3, 2),
-                "value": round(kv_bytes(wf) / (msf * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "kernel_us": {"decode_append_split": round(sf, 2),
-                              "merge_states": round(float(np.mean(segf[:, 2])) * 1e3, 2)},
-                "step": "append fused into the split kernel, then merge (2 launches)"}
-            del bf
-        for name, (wf, _, cf) in (("decode_1k_b32", make_workload("1k")),
-                                  ("decode_8k_b16", make_workload("8k"))):
-            torch.cuda.empty_cache()
-            ctl = fp16_control_line(wf, device, cf, max(10, args.steps // 2), 3, hbm_peak)
-            k16 = line["us_per_layer_step"] if name == "decode_1k_b32" else \
-                line["extra"]["decode_8k_b16"]["us_per_layer_step"]
+            ctl = fp16_control_line(wf, device, cf, n2, 3, hbm_peak)
+            ref = line["extra"][f"{name}_chunked"] if args.decode == "balanced" and \
+                f"{name}_chunked" in line["extra"] else None
+            k16 = ref["us_per_layer_step"] if ref else (
+                line["us_per_layer_step"] if name == "decode_1k_b32" else
+                line["extra"]["decode_8k_b16"]["us_per_layer_step"])
             ctl["k16v8_speedup_over_fp16_kv"] = round(ctl["us_per_layer_step"] / k16, 3)
+            ctl["compared_with"] = "K16/V8 with the same chunked split"
             line["extra"][f"{name}_fp16_kv_control"] = ctl
         torch.cuda.empty_cache()
-        line["extra"]["fullpool_40_layers"] = fullpool_line(device, 10, 3, hbm_peak)
+        line["extra"]["fullpool_40_layers"] = fullpool_line(device, 10, 3, hbm_peak,
+                                                            schedule="balanced")
+        line["extra"]["fullpool_40_layers_chunked"] = fullpool_line(device, 10, 3, hbm_peak,
+                                                                    schedule="chunked")
         _, tpeak, tkind = load_peaks()
         torch.cuda.empty_cache()
         line["extra"]["prefill"] = {
@@ -839,7 +886,7 @@ def main_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "impl": "reference", "config": config_of(w, label, chunk, 1),
+            "impl": "reference", "config": config_of(w, label, chunk, replicas_for(w), args.decode),
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": ncores, "kind": "oracle",
                              "sample": f"each step: sequences 0..{len(sample) - 1} of the "
                                        "workload (append + split partials + merge)"},

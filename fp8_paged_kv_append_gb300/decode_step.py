@@ -38,10 +38,17 @@ class MultiLayerDecode:
     k_caches[l] fp16 [P,Hkv,16,D], v_caches[l] uint8 [P,Hkv,16,D], v_scales[l]
     fp32 [Hkv]; block_table int32 [B, max_pages]; seq_lens int32 [B] (the
     lengths after this step's append); slots int64 [B] (where the new token
-    of each sequence goes)."""
+    of each sequence goes).
+
+    schedule "chunked": split-KV with a fixed split_chunk, then the merge;
+    "balanced": the load-balanced split (one full wave of equal tile ranges)
+    and its merge.  The block table and lengths are written only by host
+    copies, never by the kernel before the attention, so the balanced split
+    may read them ahead of its wait on that kernel."""
 
     def __init__(self, k_caches, v_caches, v_scales, block_table, seq_lens, slots, max_seq_len,
-                 num_qo_heads, sm_scale=None, split_chunk=512, validate=True):
+                 num_qo_heads, sm_scale=None, split_chunk=512, validate=True,
+                 schedule="chunked"):
         if validate:
             validate_scales(v_scales)
         self.k_caches, self.v_caches, self.v_scales = k_caches, v_caches, v_scales
@@ -55,19 +62,34 @@ class MultiLayerDecode:
         self.d = int(k_caches[0].shape[3])
         self.sm_scale = float(sm_scale if sm_scale is not None else 1.0 / math.sqrt(self.d))
         self.chunk = int(split_chunk)
-        n = K.k16v8_decode_workspace_size(self.batch, self.hq, self.d, self.max_seq_len,
-                                          self.chunk)
+        if schedule not in ("chunked", "balanced"):
+            raise ValueError(f"unknown schedule {schedule!r}")
+        self.schedule = schedule
+        if schedule == "balanced":
+            n = K.k16v8_decode_balanced_workspace_size(self.batch, self.hq, self.d)
+        else:
+            n = K.k16v8_decode_workspace_size(self.batch, self.hq, self.d, self.max_seq_len,
+                                              self.chunk)
         if n == 0:
             raise ValueError("invalid decode workspace shape")
         self.workspace = torch.empty(n, dtype=torch.uint8, device=dev)
-        self.partial_o, self.partial_lse = K.workspace_views(
-            self.workspace, self.batch, self.hq, self.d, self.max_seq_len, self.chunk)
+        if schedule == "chunked":
+            self.partial_o, self.partial_lse = K.workspace_views(
+                self.workspace, self.batch, self.hq, self.d, self.max_seq_len, self.chunk)
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
 
     def layer(self, li, q, k_new, v_new, out, lse=None):
         K.k16v8_kv_append(k_new, v_new, self.slots, self.v_scales[li], self.k_caches[li],
                           self.v_caches[li], self.dev_error)
+        if self.schedule == "balanced":
+            K.k16v8_paged_decode_balanced_split(q, self.k_caches[li], self.v_caches[li],
+                                                self.v_scales[li], self.block_table,
+                                                self.seq_lens, self.sm_scale, self.workspace,
+                                                out, lse, self.dev_error,
+                                                flags=K.DECODE_METADATA_READY)
+            K.k16v8_merge_balanced(self.workspace, self.hkv, out, lse)
+            return
         K.k16v8_paged_decode_split(q, self.k_caches[li], self.v_caches[li], self.v_scales[li],
                                    self.block_table, self.seq_lens, self.max_seq_len,
                                    self.sm_scale, self.chunk, self.workspace, self.dev_error)

@@ -101,3 +101,30 @@ def test_scale_validation_rejects_bad_scale(setup):
     bad[1][3] = 0.0
     with pytest.raises(ScaleError):
         validate_scales(bad)
+
+
+def test_fullpool_balanced_schedule_matches_oracle(setup):
+    """The same 40-layer step on the load-balanced split (captured graph, block
+    table and lengths read ahead of the wait on the append kernel): sampled
+    (layer, sequence) pairs against the oracle."""
+    from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
+    s = setup
+    lay, B = s["lay"], len(s["lay"].seq_lens)
+    step = MultiLayerDecode([p[0] for p in s["pools"]], [p[1] for p in s["pools"]],
+                            [p[2] for p in s["pools"]], to_dev(lay.block_table),
+                            to_dev(lay.seq_lens), to_dev(s["slots"]),
+                            int(lay.seq_lens.max()), 40, schedule="balanced")
+    outs = [torch.full((B, 40, 128), float("nan"), dtype=torch.float16, device=dev())
+            for _ in range(LAYERS)]
+    lses = [torch.full((B, 40), float("nan"), dtype=torch.float32, device=dev())
+            for _ in range(LAYERS)]
+    step.capture(s["qs"], s["kn"], s["vn"], outs, lses)
+    for o in outs:
+        o.fill_(float("nan"))
+    step.replay()
+    assert step.check() == 0
+    for l, b in s["sample"]:
+        ro, rl = oracle_for(s, l, b)
+        check_close(outs[l][b].float().cpu().numpy(), ro, lses[l][b].cpu().numpy(), rl)
+    for l in (0, 39):  # every row written (no NaN left from the fill)
+        assert not torch.isnan(outs[l]).any() and not torch.isnan(lses[l]).any()
