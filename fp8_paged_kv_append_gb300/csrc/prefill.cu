@@ -226,10 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         alpha = ex2(m_used - rmax);
         m_used = rmax;
       }
-      // O_w is stable once PV_w(j-1) has completed
-      if (j > 0) cta_wait(&bars[kBarODone + w], (j - 1) & 1, abort_flag, dev_error);
-      tc::fence_after_sync();
+      // O_w is stable once PV_w(j-1) has completed.  S_w(j) was issued after
+      // PV_w(j-1) and MMAs complete in order, so that is already so; the
+      // wait (free by now) only orders the O accesses of a rescale.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        cta_wait(&bars[kBarODone + w], (j - 1) & 1, abort_flag, dev_error);
+        tc::fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           const float2 x = __ffma2_rn(
               make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sc2, nm2);
           // 3 of every 8 pairs on the FMA pipe, the rest on MUFU
-          float2 pp = (e & 7) >= 5 ? exp2_poly(x) : make_float2(ex2(x.x), ex2(x.y));
+          float2 pp = make_float2(ex2(x.x), ex2(x.y));
           if (need_mask) {
             if (c0 > lim) pp.x = 0.f;
             if (c0 + 1 > lim) pp.y = 0.f;
