@@ -47,7 +47,7 @@ constexpr int kRows = kQTok * kGroup;       // 128 MMA rows per tile
 constexpr int kKv = 128;                    // KV positions per tile
 constexpr int kPagesPerTile = kKv / kPage;  // 8
 constexpr int kDequantWarps = 4;
-constexpr int kLoadWarp = 12, kMmaWarp = 13;
+constexpr int kLoadWarp = 12;  // warp 13 issues the MMAs
 constexpr int kThreads = 14 * 32;
 
 constexpr uint32_t kQBytes = kRows * 256;          // one Q tile: 2 K-blocks [128][64] fp16
@@ -78,31 +78,6 @@ enum {
   kBarODone = 17,   // +tile
   kNumBars = 19
 };
-
-// 2^x for a pair, on the FMA pipe (takes part of the exponentials off the
-// MUFU unit, which would otherwise bound the softmax).  Cody-Waite reduction
-// x = n + f with n = rint(x) via the 1.5*2^23 rounding constant and
-// f in [-1/2, 1/2]; 2^f by a degree-5 polynomial whose coefficients were
-// fitted here by least squares on Chebyshev nodes of [-1/2, 1/2] (max
-// relative error 2.2e-7 in fp32 Horner form); 2^n by adding n to the
-// exponent field.  Inputs below -127 give 0 (x is clamped there).
-__device__ __forceinline__ float2 exp2_poly(float2 x) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -127.f);
-  x.y = fmaxf(x.y, -127.f);
-  const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
-  const float2 r = __fadd2_rn(t, make_float2(-kRound, -kRound));  // rint(x)
-  const float2 f = __fadd2_rn(x, make_float2(-r.x, -r.y));
-  float2 p = make_float2(1.3266970636323094e-3f, 1.3266970636323094e-3f);
-  p = __ffma2_rn(p, f, make_float2(9.675459936261177e-3f, 9.675459936261177e-3f));
-  p = __ffma2_rn(p, f, make_float2(5.550742521882057e-2f, 5.550742521882057e-2f));
-  p = __ffma2_rn(p, f, make_float2(2.4022121727466583e-1f, 2.4022121727466583e-1f));
-  p = __ffma2_rn(p, f, make_float2(6.931469440460205e-1f, 6.931469440460205e-1f));
-  p = __ffma2_rn(p, f, make_float2(1.0000001192092896f, 1.0000001192092896f));
-  // t's low bits hold n (offset 0x4B400000, which vanishes after << 23)
-  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
-                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
-}
 
 // Bounded wait shared by every role.  A wait that runs out sets the
 // CTA-wide abort flag (and the device error word); later waits return at
@@ -258,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           const int c0 = c * 32 + 2 * e;
           const float2 x = __ffma2_rn(
               make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sc2, nm2);
-          // 3 of every 8 pairs on the FMA pipe, the rest on MUFU
+          // every exponential on MUFU: an FMA-pipe polynomial for part of them
+          // lengthened this latency-bound pass
           float2 pp = make_float2(ex2(x.x), ex2(x.y));
           if (need_mask) {
             if (c0 > lim) pp.x = 0.f;
