@@ -93,6 +93,24 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, volatil
   return false;
 }
 
+// Bounded poll until three barrier phases have all completed (c may be
+// null); each is tested until seen once.  Used by the MMA thread.
+__device__ __forceinline__ bool wait_all3(uint64_t *a, uint32_t pa, uint64_t *b, uint32_t pb,
+                                          uint64_t *c, uint32_t pc, volatile int *abort_flag,
+                                          int32_t *dev_error) {
+  if (*abort_flag) return false;
+  bool da = false, db = false, dc = c == nullptr;
+  for (uint32_t i = 0; i < kMaxSpins; ++i) {
+    if (!db) db = mbar_test_wait(b, pb);
+    if (!dc) dc = mbar_test_wait(c, pc);
+    if (!da) da = mbar_test_wait(a, pa);
+    if (da && db && dc) return true;
+  }
+  *abort_flag = 1;
+  flag_error(dev_error, K16V8_DEVERR_TIMEOUT);
+  return false;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const uint8_t *__restrict__ v_cache, const float *__restrict__ v_scale,
@@ -431,15 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       for (int j = 0; j < n_kv; ++j) {
         const int s = j & 1;
         const bool more = j + 1 < n_kv;
-        cta_wait(&bars[kBarPFull + 0], j & 1, abort_flag, dev_error, true);
-        cta_wait(&bars[kBarVFull + s], (j >> 1) & 1, abort_flag, dev_error, true);
+        // P_A(j), V(j) and K(j+1) in one polling loop: V and K are nearly
+        // always in place before P_A, so once P_A lands the two MMA groups
+        // go out back to back, with no wait between them.
+        wait_all3(&bars[kBarPFull + 0], j & 1, &bars[kBarVFull + s], (j >> 1) & 1,
+                  more ? &bars[kBarKFull + ((j + 1) & 1)] : nullptr, ((j + 1) >> 1) & 1,
+                  abort_flag, dev_error);
         tc::fence_after_sync();
         issue_pv(0, j);
-        if (more) {
-          cta_wait(&bars[kBarKFull + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, dev_error, true);
-          tc::fence_after_sync();
-          issue_s(0, j + 1);
-        }
+        if (more) issue_s(0, j + 1);
         cta_wait(&bars[kBarPFull + 1], j & 1, abort_flag, dev_error, true);
         tc::fence_after_sync();
         issue_pv(1, j);
