@@ -113,6 +113,7 @@ __device__ __forceinline__ bool wait_all3(uint64_t *a, uint32_t pa, uint64_t *b,
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+    const __grid_constant__ CUtensorMap tmap_o,
     const uint8_t *__restrict__ v_cache, const float *__restrict__ v_scale,
     const int32_t *__restrict__ qo_indptr, const int32_t *__restrict__ block_table, int32_t maxp,
     const int32_t *__restrict__ seq_lens, int32_t total_q, int32_t hq, int32_t hkv,
@@ -271,7 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
     pdl_launch_dependents();
     // ---- epilogue ----
-    if (cta_wait(&bars[kBarODone + w], (n_kv - 1) & 1, abort_flag, dev_error)) {
+    // A tile whose 32 tokens all belong to this sequence leaves through a
+    // TMA store from its own Q buffer (free: its last S has completed before
+    // its last P.V); a partial tile at the end of a sequence is written row
+    // by row so the next sequence's rows stay untouched.
+    const bool full_tile = t_lo + (w + 1) * kQTok <= qlen;  // uniform over the group
+    uint8_t *stage = sQ + w * kQBytes;
+    const bool o_ready = cta_wait(&bars[kBarODone + w], (n_kv - 1) & 1, abort_flag, dev_error);
+    if (o_ready) {
       tc::fence_after_sync();
       const float inv = __ldg(v_scale + g) / l;
       const int64_t orow = static_cast<int64_t>(q0 + t_abs) * hq + g * kGroup + (r & 3);
@@ -280,22 +288,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         uint32_t o[32];
         tc::tmem_ld32(tO + lane_base + c * 32, o);
         tc::tmem_wait_ld();
-        if (row_valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[4];
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __half2 hh = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
-                                                   __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
-              pk[e] = *reinterpret_cast<const uint32_t *>(&hh);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const __half2 hh = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
+                                                 __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
+            pk[e] = *reinterpret_cast<const uint32_t *>(&hh);
+          }
+          if (full_tile) {
+            // dims 32c + 8q .. +7: box half c >> 1, 16-byte chunk (c & 1) * 4 + q of row r
+            const uint32_t off = static_cast<uint32_t>(r) * 128 + ((c & 1) * 4 + q) * 16;
+            *reinterpret_cast<uint4 *>(stage + (c >> 1) * (kQBytes / 2) + tc::sw128(off)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          } else if (row_valid) {
             *reinterpret_cast<uint4 *>(out + orow * kHeadDim + c * 32 + q * 8) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
       }
       if (row_valid && lse_out) lse_out[orow] = (m_used + lg2(l)) * kLn2;
+    }
+    if (full_tile) {  // every thread of the group reaches this barrier
+      fence_proxy_async();
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + w), "r"(kRows) : "memory");
+      if (r == 0 && !*abort_flag) {
+        const int z = q0 + t_lo + w * kQTok;
+        tc::tma_store_3d(&tmap_o, stage, 0, g * kGroup, z);
+        tc::tma_store_3d(&tmap_o, stage + kQBytes / 2, 64, g * kGroup, z);
+        tc::bulk_commit();
+        tc::bulk_wait_read();  // the buffer must outlive the copy's reads
+      }
     }
   } else if (warp < 8 + kDequantWarps) {
     // ================= V dequantisation =================
@@ -562,11 +586,26 @@ extern "C" int32_t k16v8_paged_prefill_attention(
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return K16V8_ERR_CUDA;
   }
+  CUtensorMap mo;  // the output, same geometry and box as the query
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim),
+                                static_cast<cuuint64_t>(num_qo_heads),
+                                static_cast<cuuint64_t>(total_q)};
+    const cuuint64_t strides[2] = {kHeadDim * 2ull,
+                                   static_cast<cuuint64_t>(num_qo_heads) * kHeadDim * 2ull};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kGroup), static_cast<cuuint32_t>(kQTok)};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, out, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return K16V8_ERR_CUDA;
+  }
   int32_t st = set_smem_attr();
   if (st != K16V8_OK) return st;
   const dim3 grid((max_qlen + 2 * kQTok - 1) / (2 * kQTok), num_kv_heads, batch);
   return k16v8_launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes,
-                          static_cast<cudaStream_t>(stream), mq, mk, v_cache, v_scale, qo_indptr,
+                          static_cast<cudaStream_t>(stream), mq, mk, mo, v_cache, v_scale, qo_indptr,
                           block_table, max_pages_per_seq, seq_lens, total_q, num_qo_heads,
                           num_kv_heads, num_pages, sm_scale, static_cast<__half *>(out), lse,
                           dev_error);
