@@ -153,12 +153,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   const int n_kv = p_hi / kKv + 1;
   const int32_t *bt = block_table + static_cast<int64_t>(b) * maxp;
 
+  if (warp == kLoadWarp && lane == 0) {
+    // The query load depends on nothing else: start it before the rest of
+    // the set-up (its barrier is this thread's to initialise).
+    mbar_init(&bars[kBarQ], 1);
+    fence_barrier_init();
+    tc::prefetch_tensormap(&tmap_q);
+    tc::prefetch_tensormap(&tmap_k);
+    mbar_arrive_expect_tx(&bars[kBarQ], 2 * kQBytes);
+    for (int w = 0; w < 2; ++w) {
+      tc::tma_load_3d(sQ + w * kQBytes, &tmap_q, 0, g * kGroup, q0 + t_lo + w * kQTok,
+                      &bars[kBarQ]);
+      tc::tma_load_3d(sQ + w * kQBytes + kQBytes / 2, &tmap_q, 64, g * kGroup,
+                      q0 + t_lo + w * kQTok, &bars[kBarQ]);
+    }
+  }
   if (warp == 0) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
+      if (i == kBarQ) continue;  // initialised by the load warp
       uint32_t count = 1;
       if (i == kBarVstEmpty || i == kBarVstEmpty + 1 || i == kBarVFull || i == kBarVFull + 1)
         count = kDequantWarps * 32;
@@ -368,17 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       if (p < 0 || p >= num_pages) flag_error(dev_error, K16V8_DEVERR_PAGE);
     }
     __syncwarp();
-    if (lane == 0) {
-      tc::prefetch_tensormap(&tmap_q);
-      tc::prefetch_tensormap(&tmap_k);
-      mbar_arrive_expect_tx(&bars[kBarQ], 2 * kQBytes);
-      for (int w = 0; w < 2; ++w) {
-        tc::tma_load_3d(sQ + w * kQBytes, &tmap_q, 0, g * kGroup, q0 + t_lo + w * kQTok,
-                        &bars[kBarQ]);
-        tc::tma_load_3d(sQ + w * kQBytes + kQBytes / 2, &tmap_q, 64, g * kGroup,
-                        q0 + t_lo + w * kQTok, &bars[kBarQ]);
-      }
-    }
     // Per tile, lane i < 8 issues the three copies of page i; lane 0 first
     // posts the tile's byte count on both barriers.
     for (int j = 0; j < n_kv; ++j) {
