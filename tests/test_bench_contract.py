@@ -1,0 +1,43 @@
+"""bench.py's reference arm on the CPU: one JSON line with the contract's
+keys, on the same metric and config as the GPU arm."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "1"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "impl",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+    # same metric and config as the GPU arm's default line
+    sys.path.insert(0, ROOT)
+    import bench
+    w, label, chunk = bench.make_workload("1k")
+    assert d["metric"] == bench.METRIC
+    assert d["config"] == bench.config_of(w, label, chunk, bench.replicas_for(w), "balanced")
+
+
+def test_replicas_cover_four_l2():
+    sys.path.insert(0, ROOT)
+    import bench
+    for name in ("1k", "8k"):
+        w, _, _ = bench.make_workload(name)
+        pool = w.num_pages * w.num_kv_heads * 16 * w.head_dim * 3
+        assert bench.replicas_for(w) * pool >= 4 * bench.L2_BYTES
