@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
     for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
 
   const int j = lane & 7;
-  uint32_t qh[kGroup][8];
-  load_group_query(q + (static_cast<int64_t>(b) * hq + g * kGroup) * kHeadDim, j, qh);
+  uint32_t qf[16];
+  load_group_query(q + (static_cast<int64_t>(b) * hq + g * kGroup) * kHeadDim, qf);
   const float qs = sm_scale * kLog2e;  // scores in the log2 domain
 
   const int hsel = j >> 1;  // head whose score this lane holds
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
       }
       __syncwarp();
     }
-    if (page_ids[i] >= 0) attend_page<kVF16>(ring, s, valid, qh, qs, st);
+    if (page_ids[i] >= 0) attend_page<kVF16>(ring, s, valid, qf, qs, st);
     __syncwarp();
     if (lane == 0 && k + kStages < n_my) {
       fence_proxy_async();
@@ -175,10 +175,8 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
 
   pdl_launch_dependents();
 
-  // ---- sum each head's l over its lanes (lanes j, j^1 hold copies) ----
-  float l_run = st.l;
-  l_run += __shfl_xor_sync(kFull, l_run, 8);
-  l_run += __shfl_xor_sync(kFull, l_run, 16);
+  st.finish();  // m, l of head hsel in every lane
+  const float l_run = st.l;
 
   // ---- combine the four warps in shared memory (ring 0's K tiles) ----
   __syncthreads();

@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(kWarps * 32, kBalCtasPerSm) decode_balanced_ke
   bool ok = true;
   int piece = 0;
   while (true) {
-    uint32_t qh[kGroup][8];
-    load_group_query(q + (static_cast<int64_t>(cs.b) * hq + cs.g * kGroup) * kHeadDim, j, qh);
+    uint32_t qf[16];
+    load_group_query(q + (static_cast<int64_t>(cs.b) * hq + cs.g * kGroup) * kHeadDim, qf);
     WarpState st;
     st.reset();
     const int seg_end = cs.s0 + cs.np;
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kWarps * 32, kBalCtasPerSm) decode_balanced_ke
       if (ok) {
         if (ring.live[s]) {
           const int valid = min(kPage, cs.L - (fc - cs.s0) * kPage);
-          attend_page<false>(ring, s, valid, qh, qs, st);
+          attend_page<false>(ring, s, valid, qf, qs, st);
         }
         __syncwarp();
         if (ki < n_my) {
@@ -302,9 +302,8 @@ __global__ void __launch_bounds__(kWarps * 32, kBalCtasPerSm) decode_balanced_ke
     if (last) pdl_launch_dependents();
 
     // ---- combine the four warps' states for this piece ----
-    float l_run = st.l;
-    l_run += __shfl_xor_sync(kFull, l_run, 8);
-    l_run += __shfl_xor_sync(kFull, l_run, 16);
+    st.finish();  // m, l of head hsel in every lane
+    const float l_run = st.l;
     if (warp > 0) {
       if (piece > 0) named_bar_sync(2, kWarps * 32);  // warp 0 has read the last staging
 #pragma unroll

@@ -6,11 +6,16 @@
 // keys, E4M3 values with a per-(layer, KV head) FP32 scale, 40 query heads
 // over 10 KV heads, d = 128, 16-token pages.
 //
-//  * Q.K: eight lanes own one token (16 dims each, conflict-free 16-byte
-//    shared loads), fp16-operand FMAs with fp32 accumulation against the
-//    query held as packed fp16 pairs, then a 3-step reduce-scatter so each
-//    lane ends with one (token, head) score: 4 shuffles per 4 tokens.
-//  * Online softmax in the log2 domain per page (running max / sum).
+//  * Q.K on the tensor core: one m16n8k16 MMA per 16 dims (fp16 operands,
+//    fp32 accumulation) with the page's 16 tokens as M and the 4 heads
+//    (padded to 8 with zero columns) as N, so the scores land one (token,
+//    head) per accumulator register.  Each lane owns the same 32 dims of
+//    the key rows (tokens g, g + 8) and of the query column (head g); the
+//    dot product does not depend on how dims are assigned to the MMA's K
+//    index, only that key and query use the same assignment.
+//  * Online softmax in the log2 domain per page (running max / sum), on the
+//    accumulator layout: lanes 4g + t (t < 2) hold heads 2t, 2t + 1 of
+//    tokens g and g + 8.
 //  * P.V: each lane owns 4 dims of every token; E4M3 -> fp16 pairs by the
 //    hardware cvt, fp16x2 FMAs summed over one 16-token page (p <= 1 and
 //    |v| <= 448 keep a page sum below 7168), folded into fp32 state per
@@ -43,66 +48,67 @@ struct __align__(128) WarpRingT {
 using WarpRing = WarpRingT<kVPageBytes>;        // E4M3 values
 using WarpRing16 = WarpRingT<2 * kVPageBytes>;  // FP16 values (the FP16-KV control)
 
-// acc += a.lo * b.lo + a.hi * b.hi with fp16 operands, fp32 accumulation
-// (each product is exact in fp32; one rounding per FMA).
-__device__ __forceinline__ float fma_h2(uint32_t a, uint32_t b, float acc) {
-  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
-      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
-      "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(a), "r"(b));
-  return acc;
+// d += A (16x16, row-major fp16) * B (16x8, column-major fp16), fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Sum acc[0..3] over the 8 lanes of a token group; lane j of the group ends
-// with the total of head j >> 1.
-__device__ __forceinline__ float reduce_scatter8(const float (&acc)[kGroup], int j) {
-  const bool up4 = j & 4;
-  const float s0 = up4 ? acc[0] : acc[2];
-  const float s1 = up4 ? acc[1] : acc[3];
-  float k0 = up4 ? acc[2] : acc[0];
-  float k1 = up4 ? acc[3] : acc[1];
-  k0 += __shfl_xor_sync(kFull, s0, 4);
-  k1 += __shfl_xor_sync(kFull, s1, 4);
-  const bool up2 = j & 2;
-  const float snd = up2 ? k0 : k1;
-  float kp = up2 ? k1 : k0;
-  kp += __shfl_xor_sync(kFull, snd, 2);
-  kp += __shfl_xor_sync(kFull, kp, 1);
-  return kp;
-}
+// The 16-byte chunks of a 128-dim fp16 row owned by lane group t (= lane & 3):
+// dims [16t, 16t+16) and [64+16t, 64+16t+16).  Word w (= 2 dims) of the
+// concatenated chunks feeds K index pair (w & 1 ? 2t+8 : 2t) of MMA step w / 2.
+__device__ __forceinline__ int qk_chunk(int i, int t) { return (i >> 1) * 8 + 2 * t + (i & 1); }
 
-// Query of the group's 4 heads as packed fp16 pairs.  Lane j (= lane & 7) of
-// a token group owns dims [8j, 8j+8) and [64+8j, 64+8j+8): qh[h][0..3],
-// qh[h][4..7].  `qb` points at the group's first head row.
-__device__ __forceinline__ void load_group_query(const __half *qb, int j,
-                                                 uint32_t (&qh)[kGroup][8]) {
+// Query of the group's 4 heads as the MMA's B operand: lane 4g + t holds the
+// 16 words of head g's dims (zero for g >= 4, the padding columns).
+// `qb` points at the group's first head row.
+__device__ __forceinline__ void load_group_query(const __half *qb, uint32_t (&qf)[16]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
-  for (int h = 0; h < kGroup; ++h) {
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      const uint4 raw =
-          __ldg(reinterpret_cast<const uint4 *>(qb + h * kHeadDim + part * 64 + j * 8));
-      qh[h][part * 4 + 0] = raw.x;
-      qh[h][part * 4 + 1] = raw.y;
-      qh[h][part * 4 + 2] = raw.z;
-      qh[h][part * 4 + 3] = raw.w;
-    }
+  for (int i = 0; i < 4; ++i) {
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (g < kGroup)
+      raw = __ldg(reinterpret_cast<const uint4 *>(qb + g * kHeadDim) + qk_chunk(i, t));
+    qf[4 * i + 0] = raw.x;
+    qf[4 * i + 1] = raw.y;
+    qf[4 * i + 2] = raw.z;
+    qf[4 * i + 3] = raw.w;
   }
 }
 
-// Running attention state of one warp for the 4 heads of a group: m / l for
-// head (lane & 7) >> 1 (every lane holding that head has the same value once
-// l is summed over the lanes), o for dims [4*lane, 4*lane+4) of each head.
+// Running attention state of one warp for the 4 heads of a group.  During
+// the page loop: mh / lh for heads 2t, 2t+1 (t = lane & 3 < 2), lh summed
+// over this lane's tokens only; o for dims [4*lane, 4*lane+4) of each head.
+// After finish(): m and l (summed over the page tokens) for head
+// (lane & 7) >> 1 in every lane.
 struct WarpState {
   float m, l;
+  float mh[2], lh[2];
   float2 o[kGroup][2];
   __device__ __forceinline__ void reset() {
-    m = -INFINITY;
-    l = 0.f;
+    mh[0] = mh[1] = -INFINITY;
+    lh[0] = lh[1] = 0.f;
 #pragma unroll
     for (int h = 0; h < kGroup; ++h) o[h][0] = o[h][1] = make_float2(0.f, 0.f);
+  }
+  __device__ __forceinline__ void finish() {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      lh[e] += __shfl_xor_sync(kFull, lh[e], 4);
+      lh[e] += __shfl_xor_sync(kFull, lh[e], 8);
+      lh[e] += __shfl_xor_sync(kFull, lh[e], 16);
+    }
+    const int hsel = (lane & 7) >> 1;  // held by lane hsel >> 1, element hsel & 1
+    const float m0 = __shfl_sync(kFull, mh[0], hsel >> 1);
+    const float m1 = __shfl_sync(kFull, mh[1], hsel >> 1);
+    const float l0 = __shfl_sync(kFull, lh[0], hsel >> 1);
+    const float l1 = __shfl_sync(kFull, lh[1], hsel >> 1);
+    m = (hsel & 1) ? m1 : m0;
+    l = (hsel & 1) ? l1 : l0;
   }
 };
 
@@ -110,53 +116,60 @@ struct WarpState {
 // warp's state.  qs = softmax scale * log2(e).
 template <bool kVF16, typename Ring>
 __device__ __forceinline__ void attend_page(Ring &ring, int s, int valid,
-                                            const uint32_t (&qh)[kGroup][8], float qs,
+                                            const uint32_t (&qf)[16], float qs,
                                             WarpState &st) {
   const int lane = threadIdx.x & 31;
-  const int j = lane & 7;
-  const int hsel = j >> 1;
-  // ---- scores of 16 tokens x 4 heads ----
+  const int g = lane >> 2, t = lane & 3;
+  // ---- scores: S[token][head] = K Q^T, tokens g / g+8 x heads 2t, 2t+1 ----
   const uint8_t *kp = ring.k[s];
-  float sc[4];
+  uint4 ka[4], kb[4];
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int t = it * 4 + (lane >> 3);
-    const uint4 a = *reinterpret_cast<const uint4 *>(kp + t * 256 + j * 16);
-    const uint4 bq = *reinterpret_cast<const uint4 *>(kp + t * 256 + 128 + j * 16);
-    float acc[kGroup], acc2[kGroup];
+  for (int i = 0; i < 4; ++i) {
+    ka[i] = *reinterpret_cast<const uint4 *>(kp + g * 256 + qk_chunk(i, t) * 16);
+    kb[i] = *reinterpret_cast<const uint4 *>(kp + (g + 8) * 256 + qk_chunk(i, t) * 16);
+  }
+  float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int h = 0; h < kGroup; ++h) {
-      acc[h] = fma_h2(qh[h][0], a.x, 0.f);
-      acc2[h] = fma_h2(qh[h][4], bq.x, 0.f);
-      acc[h] = fma_h2(qh[h][1], a.y, acc[h]);
-      acc2[h] = fma_h2(qh[h][5], bq.y, acc2[h]);
-      acc[h] = fma_h2(qh[h][2], a.z, acc[h]);
-      acc2[h] = fma_h2(qh[h][6], bq.z, acc2[h]);
-      acc[h] = fma_h2(qh[h][3], a.w, acc[h]);
-      acc2[h] = fma_h2(qh[h][7], bq.w, acc2[h]);
-      acc[h] += acc2[h];
-    }
-    const float v = reduce_scatter8(acc, j) * qs;
-    sc[it] = t < valid ? v : -INFINITY;
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint4 &x = ka[ks >> 1], &y = kb[ks >> 1];
+    if (ks & 1)
+      mma_16816(sacc, x.z, y.z, x.w, y.w, qf[2 * ks], qf[2 * ks + 1]);
+    else
+      mma_16816(sacc, x.x, y.x, x.y, y.y, qf[2 * ks], qf[2 * ks + 1]);
   }
   // ---- online softmax (log2 domain) ----
-  float pm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-  pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 8));
-  pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 16));
-  const float m_new = fmaxf(st.m, pm);
-  const float alpha = ex2(st.m - m_new);
-  float p[4];
+  float sc[4];
+  sc[0] = g < valid ? sacc[0] * qs : -INFINITY;
+  sc[1] = g < valid ? sacc[1] * qs : -INFINITY;
+  sc[2] = g + 8 < valid ? sacc[2] * qs : -INFINITY;
+  sc[3] = g + 8 < valid ? sacc[3] * qs : -INFINITY;
+  float pm[2] = {fmaxf(sc[0], sc[2]), fmaxf(sc[1], sc[3])};
 #pragma unroll
-  for (int it = 0; it < 4; ++it) p[it] = ex2(sc[it] - m_new);
-  st.l = st.l * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
-  st.m = m_new;
-  if ((lane & 1) == 0) {
+  for (int e = 0; e < 2; ++e) {
+    pm[e] = fmaxf(pm[e], __shfl_xor_sync(kFull, pm[e], 4));
+    pm[e] = fmaxf(pm[e], __shfl_xor_sync(kFull, pm[e], 8));
+    pm[e] = fmaxf(pm[e], __shfl_xor_sync(kFull, pm[e], 16));
+  }
+  float alpha[2], p[4];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const uint32_t ph = __half_as_ushort(__float2half_rn(p[it]));
-      ring.p[(it * 4 + (lane >> 3)) * kGroup + hsel] = ph | (ph << 16);
+  for (int e = 0; e < 2; ++e) {
+    const float m_new = fmaxf(st.mh[e], pm[e]);  // finite: token 0 is valid
+    alpha[e] = ex2(st.mh[e] - m_new);
+    p[e] = ex2(sc[e] - m_new);
+    p[e + 2] = ex2(sc[e + 2] - m_new);
+    st.lh[e] = st.lh[e] * alpha[e] + (p[e] + p[e + 2]);
+    st.mh[e] = m_new;
+  }
+  if (t < 2) {
+    uint32_t ph[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ph[e] = __half_as_ushort(__float2half_rn(p[e]));
+      ph[e] |= ph[e] << 16;
     }
-    if (lane < 8) ring.alpha[hsel] = alpha;
+    *reinterpret_cast<uint2 *>(ring.p + g * kGroup + 2 * t) = make_uint2(ph[0], ph[1]);
+    *reinterpret_cast<uint2 *>(ring.p + (g + 8) * kGroup + 2 * t) = make_uint2(ph[2], ph[3]);
+    if (g == 0) *reinterpret_cast<float2 *>(ring.alpha + 2 * t) = make_float2(alpha[0], alpha[1]);
   }
   __syncwarp();
   // ---- P.V over this page: lane owns 4 dims of every token ----
@@ -164,18 +177,18 @@ __device__ __forceinline__ void attend_page(Ring &ring, int s, int valid,
 #pragma unroll
   for (int h = 0; h < kGroup; ++h) acc[h][0] = acc[h][1] = __float2half2_rn(0.f);
   const uint8_t *vp = ring.v[s] + lane * (kVF16 ? 8 : 4);
-  auto pv_token = [&](int t) {
+  auto pv_token = [&](int tok) {
     __half2 v01, v23;
     if constexpr (kVF16) {
-      const uint2 raw = *reinterpret_cast<const uint2 *>(vp + t * kHeadDim * 2);
+      const uint2 raw = *reinterpret_cast<const uint2 *>(vp + tok * kHeadDim * 2);
       v01 = *reinterpret_cast<const __half2 *>(&raw.x);
       v23 = *reinterpret_cast<const __half2 *>(&raw.y);
     } else {
-      const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp + t * kHeadDim);
+      const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp + tok * kHeadDim);
       v01 = e4m3x2_to_half2(static_cast<uint16_t>(raw & 0xffffu));
       v23 = e4m3x2_to_half2(static_cast<uint16_t>(raw >> 16));
     }
-    const uint4 pp = *reinterpret_cast<const uint4 *>(ring.p + t * kGroup);
+    const uint4 pp = *reinterpret_cast<const uint4 *>(ring.p + tok * kGroup);
     const uint32_t pw[kGroup] = {pp.x, pp.y, pp.z, pp.w};
 #pragma unroll
     for (int h = 0; h < kGroup; ++h) {
@@ -186,9 +199,9 @@ __device__ __forceinline__ void attend_page(Ring &ring, int s, int valid,
   };
   if (valid == kPage) {
 #pragma unroll
-    for (int t = 0; t < kPage; ++t) pv_token(t);
+    for (int tok = 0; tok < kPage; ++tok) pv_token(tok);
   } else {
-    for (int t = 0; t < valid; ++t) pv_token(t);
+    for (int tok = 0; tok < valid; ++tok) pv_token(tok);
   }
   // fold the page into the fp32 state: o = o * alpha + page sum
   const float4 al = *reinterpret_cast<const float4 *>(ring.alpha);

@@ -168,6 +168,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                       q0 + t_lo + w * kQTok, &bars[kBarQ]);
     }
   }
+  if (warp == kLoadWarp) {
+    // this pair's page ids into shared memory (lane-parallel), overlapping
+    // the tensor-memory and barrier set-up of the other warps
+    const int n_ids = min(n_kv * kPagesPerTile, (L + kPage - 1) / kPage);
+    for (int i = lane; i < min(n_ids, kMaxIdPages); i += 32) {
+      const int p = __ldg(bt + i);
+      page_ids[i] = (p >= 0 && p < num_pages) ? p : -1;
+      if (p < 0 || p >= num_pages) flag_error(dev_error, K16V8_DEVERR_PAGE);
+    }
+  }
   if (warp == 0) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
@@ -376,14 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
   } else if (warp == kLoadWarp) {
     // ================= loads =================
-    // stage this pair's page ids in shared memory (lane-parallel)
-    const int n_ids = min(n_kv * kPagesPerTile, (L + kPage - 1) / kPage);
-    for (int i = lane; i < min(n_ids, kMaxIdPages); i += 32) {
-      const int p = __ldg(bt + i);
-      page_ids[i] = (p >= 0 && p < num_pages) ? p : -1;
-      if (p < 0 || p >= num_pages) flag_error(dev_error, K16V8_DEVERR_PAGE);
-    }
-    __syncwarp();
+    // (page ids were staged before the set-up barrier)
     // Per tile, lane i < 8 issues the three copies of page i; lane 0 first
     // posts the tile's byte count on both barriers.
     for (int j = 0; j < n_kv; ++j) {
