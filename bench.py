@@ -126,10 +126,18 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+MODES = ("chunked", "fused", "balanced", "balanced_fused")
+DEFAULT_DECODE = "balanced_fused"  # schedule of the headline line
+SUFFIX = {"chunked": "chunked", "fused": "fused_append", "balanced": "balanced",
+          "balanced_fused": "balanced_fused_append"}
+
 KERNEL_SOURCES = {
     "chunked": ("decode_split_1k_b32.md", ["decode.cu", "decode_page.cuh", "k16v8_device.cuh"]),
     "balanced": ("decode_balanced_1k_b32.md",
                  ["decode_balanced.cu", "decode_page.cuh", "k16v8_device.cuh"]),
+    "balanced_fused": ("decode_balanced_append_1k_b32.md",
+                       ["decode_balanced.cu", "decode_page.cuh", "k16v8_device.cuh"]),
+    "fused": ("decode_split_append_1k_b32.md", ["decode.cu", "decode_page.cuh", "k16v8_device.cuh"]),
 }
 
 
@@ -174,15 +182,17 @@ class DecodeBench:
 
     def __init__(self, w, device, split_chunk=512, replicas=None, mode="chunked"):
         """mode: "chunked" (append, split, merge), "fused" (append fused into
-        the split kernel, merge) or "balanced" (append, load-balanced split,
-        its merge)."""
+        the split kernel, merge), "balanced" (append, load-balanced split,
+        its merge) or "balanced_fused" (append fused into the load-balanced
+        split, its merge)."""
         import torch
         from fp8_paged_kv_append_gb300 import k16v8 as K
-        assert mode in ("chunked", "fused", "balanced")
+        assert mode in MODES
         self.K, self.torch, self.w, self.dev = K, torch, w, device
         self.chunk = split_chunk
         self.mode = mode
-        self.fused = mode == "fused"
+        self.fused = mode in ("fused", "balanced_fused")
+        self.balanced = mode in ("balanced", "balanced_fused")
         self.R = replicas or replicas_for(w)
         P = w.num_pages
         self.P = P
@@ -208,7 +218,7 @@ class DecodeBench:
         self.q = td(w.q)
         self.seq_lens = td(w.seq_lens)
         self.max_len = int(w.seq_lens.max())
-        if mode == "balanced":
+        if self.balanced:
             self.ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d),
                                   dtype=torch.uint8, device=device)
         else:
@@ -244,6 +254,12 @@ class DecodeBench:
                                               self.v_scale, self.bt[r], self.seq_lens,
                                               self.max_len, self.w.sm_scale, self.chunk, self.ws,
                                               self.err)
+        elif self.mode == "balanced_fused":
+            # block table and lengths are never written by the preceding kernel
+            K.k16v8_paged_decode_append_balanced_split(
+                self.q, self.k_new16, self.v_new16, self.kc, self.vc, self.v_scale, self.bt[r],
+                self.seq_lens, self.w.sm_scale, self.ws, self.out, self.lse, self.err,
+                flags=K.DECODE_METADATA_READY)
         elif self.mode == "balanced":
             # block table and lengths are never written by the preceding kernel
             K.k16v8_paged_decode_balanced_split(self.q, self.kc, self.vc, self.v_scale,
@@ -257,7 +273,7 @@ class DecodeBench:
 
     def merge(self):
         K = self.K
-        if self.mode == "balanced":
+        if self.balanced:
             K.k16v8_merge_balanced(self.ws, self.w.num_kv_heads, self.out, self.lse)
         else:
             K.k16v8_merge_states(self.po, self.pl, self.seq_lens, self.chunk, self.out, self.lse)
@@ -380,6 +396,13 @@ class DecodeBench:
 
         def one(i):
             d_in.copy_(h_in[i % self.R], non_blocking=True)
+            if self.mode == "balanced_fused":
+                K.k16v8_paged_decode_append_attention_balanced(
+                    d["q"], d["k_new"], d["v_new"], self.kc, self.vc, self.v_scale, d["bt"],
+                    d["seq_lens"], w.sm_scale, self.ws, out, lse, self.err,
+                    flags=K.DECODE_METADATA_READY)
+                h_out.copy_(d_out, non_blocking=True)
+                return
             K.k16v8_kv_append(d["k_new"], d["v_new"], d["slots"], self.v_scale, self.kc,
                               self.vc, self.err)
             if self.mode == "balanced":
@@ -624,12 +647,14 @@ def fullpool_line(device, steps, warmup, hbm_peak, layers=40, schedule="chunked"
     return {"workload": f"full pool: {layers} layers x {P} pages (223,696 slots, 32 GiB), batch "
                         f"{B}, seq_lens {int(L.min())}..{int(L.max())} (sum {int(L.sum())}, "
                         f"{lay.draws} draw(s)), "
-                        + ("split 512" if schedule == "chunked" else "load-balanced split")
-                        + ", one CUDA graph per step",
+                        + {"chunked": "split 512", "fused": "split 512 with the append folded in",
+                           "balanced": "load-balanced split",
+                           "balanced_fused": "load-balanced split with the append folded in"}
+                        [schedule] + ", one CUDA graph per step",
             "ms_per_step": round(ms, 4), "us_per_layer_step": round(ms * 1e3 / layers, 2),
             "kv_bytes_per_step": kvb, "value": round(kvb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
-            "gpu_launches_per_step": 3 * layers}
+            "gpu_launches_per_step": (2 if schedule in ("fused", "balanced_fused") else 3) * layers}
 
 
 # ---- CPU baseline: the oracle on the host cores -------------------------------------
@@ -684,9 +709,13 @@ def make_workload(name):
 
 
 def config_of(w, label, chunk, replicas, mode="balanced"):
-    sched = ("load-balanced split: one full wave (SMs x 4 CTAs) of equal (sequence, KV head, "
-             "page) tile ranges, LSE merge of cut segments") if mode == "balanced" else \
-        f"split-KV chunks of {chunk} tokens, LSE merge"
+    if mode in ("balanced", "balanced_fused"):
+        sched = ("load-balanced split: one full wave (SMs x 4 CTAs) of equal (sequence, KV "
+                 "head, page) tile ranges, LSE merge of cut segments")
+    else:
+        sched = f"split-KV chunks of {chunk} tokens, LSE merge"
+    if mode in ("fused", "balanced_fused"):
+        sched += "; the new token's cache append folded into the split kernel"
     return {"workload": f"Phi-4-shaped {label}: one layer, 40 q / 10 KV heads, head_dim 128, "
                         "16-token pages, FP16 K + E4M3 V",
             "batch": int(w.batch), "seq_lens": f"{int(w.seq_lens.min())}..{int(w.seq_lens.max())}",
@@ -698,6 +727,8 @@ KERNEL_NAMES = {
     "chunked": ("decode_split", "merge_states", "decode_split_kernel"),
     "balanced": ("decode_balanced", "merge_balanced", "decode_balanced_kernel"),
     "fused": ("decode_append_split", "merge_states", "decode_split_kernel<append>"),
+    "balanced_fused": ("decode_append_balanced", "merge_balanced",
+                       "decode_balanced_kernel<append>"),
 }
 
 
@@ -718,7 +749,7 @@ def decode_line(w, label, chunk, mode, device, steps, hbm_peak):
            "split_frac_of_hbm_peak": round(sb / (s_us * 1e-6) / 1e9 / hbm_peak, 4),
            "step_frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
            "config": config_of(w, label, chunk, b.R, mode)}
-    if mode == "fused":
+    if mode in ("fused", "balanced_fused"):
         del out["kernel_us"]["kv_append"]
         out["step"] = "append fused into the split kernel, then merge (2 launches)"
     del b
@@ -737,7 +768,7 @@ def main():
                     help="skip the secondary 8K/b16 line inside the JSON")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--decode", default="balanced", choices=["chunked", "balanced"],
+    ap.add_argument("--decode", default=DEFAULT_DECODE, choices=list(MODES),
                     help="decode schedule of the main line")
     ap.add_argument("--split-chunk", type=int, default=0,
                     help="tokens per split-KV chunk of the main workload (0: its default)")
@@ -806,33 +837,31 @@ def main():
         "e2e": {"value": round(units / (te_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(te_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (2 if args.decode in ("fused", "balanced_fused") else 3) * args.steps,
         "clocks": clk,
     }
+    if args.decode in ("fused", "balanced_fused"):
+        del line["kernel_us"]["kv_append"]
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = run_cpu_baseline(w, chunk, args.cpu_budget)
     if not args.no_extra and args.workload == "1k":
         from fp8_paged_kv_append_gb300 import workloads
         del bench
         torch.cuda.empty_cache()
-        other = "chunked" if args.decode == "balanced" else "balanced"
         n2 = max(10, args.steps // 2)
         w8, label8, chunk8 = make_workload("8k")
+        wls = (("decode_1k_b32", (w, label, chunk)), ("decode_8k_b16", (w8, label8, chunk8)))
         line["extra"] = {
-            "decode_8k_b16": decode_line(w8, label8, chunk8, args.decode, device, n2, hbm_peak),
-            f"decode_1k_b32_{other}": decode_line(w, label, chunk, other, device, n2, hbm_peak),
-            f"decode_8k_b16_{other}": decode_line(w8, label8, chunk8, other, device, n2,
-                                                  hbm_peak)}
-        for name, (wf, lf, cf) in (("decode_1k_b32", (w, label, chunk)),
-                                   ("decode_8k_b16", (w8, label8, chunk8))):
-            line["extra"][f"{name}_fused_append"] = decode_line(wf, lf, cf, "fused", device, n2,
-                                                                hbm_peak)
-        for name, (wf, _, cf) in (("decode_1k_b32", (w, label, chunk)),
-                                  ("decode_8k_b16", (w8, label8, chunk8))):
+            "decode_8k_b16": decode_line(w8, label8, chunk8, args.decode, device, n2, hbm_peak)}
+        for m in MODES:
+            if m != args.decode:
+                for name, (wf, lf, cf) in wls:
+                    line["extra"][f"{name}_{SUFFIX[m]}"] = decode_line(wf, lf, cf, m, device,
+                                                                       n2, hbm_peak)
+        for name, (wf, _, cf) in wls:
             torch.cuda.empty_cache()
             ctl = fp16_control_line(wf, device, cf, n2, 3, hbm_peak)
-            ref = line["extra"][f"{name}_chunked"] if args.decode == "balanced" and \
-                f"{name}_chunked" in line["extra"] else None
+            ref = line["extra"].get(f"{name}_chunked")
             k16 = ref["us_per_layer_step"] if ref else (
                 line["us_per_layer_step"] if name == "decode_1k_b32" else
                 line["extra"]["decode_8k_b16"]["us_per_layer_step"])
@@ -841,9 +870,11 @@ def main():
             line["extra"][f"{name}_fp16_kv_control"] = ctl
         torch.cuda.empty_cache()
         line["extra"]["fullpool_40_layers"] = fullpool_line(device, 10, 3, hbm_peak,
-                                                            schedule="balanced")
-        line["extra"]["fullpool_40_layers_chunked"] = fullpool_line(device, 10, 3, hbm_peak,
-                                                                    schedule="chunked")
+                                                            schedule=args.decode)
+        for m in MODES:
+            if m != args.decode:
+                line["extra"][f"fullpool_40_layers_{SUFFIX[m]}"] = fullpool_line(
+                    device, 10, 3, hbm_peak, schedule=m)
         _, tpeak, tkind = load_peaks()
         torch.cuda.empty_cache()
         line["extra"]["prefill"] = {

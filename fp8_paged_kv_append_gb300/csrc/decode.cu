@@ -124,36 +124,13 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
     if (!ok) break;
     const int i = warp + k * kWarps;  // page within the chunk
     const int valid = min(kPage, n_tok - i * kPage);
-    if (kAppend && i == patch_page) {
-      // Quantise the new token, store it in the cache, and put the same row
-      // into the staged copy of the page (the copy may predate the store).
-      if (lane < kHeadDim / 8) {
-        const int row = (L - 1) % kPage;
-        const int64_t src = (static_cast<int64_t>(b) * hkv + g) * kHeadDim + lane * 8;
-        const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
-        const uint4 vraw = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
-        const __half2 *vh = reinterpret_cast<const __half2 *>(&vraw);
-        const float sc = __ldg(v_scale + g);
-        uint32_t w[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float2 a = __half22float2(vh[2 * u]);
-          const float2 bb = __half22float2(vh[2 * u + 1]);
-          w[u] = static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc))) |
-                 (static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(bb.x, sc), __fdiv_rn(bb.y, sc)))
-                  << 16);
-        }
-        *reinterpret_cast<uint4 *>(ring.k[s] + row * 256 + lane * 16) = kv;
-        *reinterpret_cast<uint2 *>(ring.v[s] + row * kHeadDim + lane * 8) = make_uint2(w[0], w[1]);
+    if constexpr (kAppend) {
+      if (i == patch_page) {
+        const int64_t src = (static_cast<int64_t>(b) * hkv + g) * kHeadDim;
         const int pid = page_ids[i];
-        if (pid >= 0) {
-          const int64_t dst =
-              ((static_cast<int64_t>(pid) * hkv + g) * kPage + row) * kHeadDim + lane * 8;
-          *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
-          *reinterpret_cast<uint2 *>(v_cache + dst) = make_uint2(w[0], w[1]);
-        }
+        append_new_row(ring, s, (L - 1) % kPage, k_new + src, v_new + src, __ldg(v_scale + g),
+                       k_cache, v_cache, pid >= 0 ? static_cast<int64_t>(pid) * hkv + g : -1);
       }
-      __syncwarp();
     }
     if (page_ids[i] >= 0) attend_page<kVF16>(ring, s, valid, qf, qs, st);
     __syncwarp();

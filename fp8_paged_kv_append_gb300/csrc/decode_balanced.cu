@@ -30,6 +30,11 @@
 //  * The merge kernel rebuilds, per (sequence, query head), which CTAs cut
 //    the segment and combines their partials; segments that one CTA held
 //    whole are skipped, empty sequences get a zero row and LSE -inf.
+//  * kAppend: the decode step's cache write folded in -- the warp that
+//    consumes the page holding position L - 1 of a (b, g) segment quantises
+//    the new token, stores it in the cache and in its staged copy of the
+//    page before attending to it (each page of each head is one tile, held
+//    by exactly one warp of the grid).
 #include "decode_page.cuh"
 
 namespace k16v8 {
@@ -37,6 +42,7 @@ namespace k16v8 {
 constexpr int kBalCtasPerSm = kMinBlocks;
 constexpr int kBalMinTiles = kWarps;  // at least one tile per warp
 constexpr int kBalMaxBatch = 8192;    // the scan's page offsets live in the ring space
+constexpr int kPrefetchTiles = 2;      // per warp, into L2 before the dependency wait
 
 // Cross-warp combine staging (warps 1..3) plus a few scalars.
 struct BalStage {
@@ -97,13 +103,15 @@ struct Segment {
   }
 };
 
+template <bool kAppend>
 __global__ void __launch_bounds__(kWarps * 32, kBalCtasPerSm) decode_balanced_kernel(
-    const __half *__restrict__ q, const __half *__restrict__ k_cache,
-    const uint8_t *__restrict__ v_cache, const float *__restrict__ v_scale,
+    const __half *__restrict__ q, __half *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+    const float *__restrict__ v_scale,
     const int32_t *__restrict__ block_table, int32_t maxp, const int32_t *__restrict__ seq_lens,
     int32_t batch, int32_t hq, int32_t hkv, int32_t num_pages, float sm_scale,
     int32_t *__restrict__ plan, float *__restrict__ part_o, float *__restrict__ part_lse,
-    __half *__restrict__ out, float *__restrict__ lse_out, int32_t *dev_error, int32_t flags) {
+    __half *__restrict__ out, float *__restrict__ lse_out, const __half *__restrict__ k_new,
+    const __half *__restrict__ v_new, int32_t *dev_error, int32_t flags) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   WarpRing *rings = reinterpret_cast<WarpRing *>(smem_raw);
   BalStage &stg = *reinterpret_cast<BalStage *>(smem_raw + kWarps * sizeof(WarpRing));
@@ -217,6 +225,13 @@ __global__ void __launch_bounds__(kWarps * 32, kBalCtasPerSm) decode_balanced_ke
     desc_cur = describe(0, walk, true);
     if (n_my > 32) desc_nxt = describe(32, walk, false);
   }
+  if (early && lane < kPrefetchTiles && desc_cur >= 0) {
+    // While the preceding kernel finishes, start this warp's first pages on
+    // their way into L2 (the copies into shared memory wait below).
+    const int64_t off = static_cast<int64_t>(desc_cur) * kPage * kHeadDim;
+    bulk_prefetch_l2(k_cache + off, kKPageBytes);
+    bulk_prefetch_l2(v_cache + off, kVPageBytes);
+  }
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) mbar_init(&stg.bar[warp][s], 1);
@@ -248,7 +263,7 @@ __global__ void __launch_bounds__(kWarps * 32, kBalCtasPerSm) decode_balanced_ke
         ring.live[s] = 0;
         mbar_arrive(&bars[s]);  // nothing to load: complete the phase empty
       } else {
-        ring.live[s] = 1;
+        ring.live[s] = t + 1;  // t < 2^31 - 1 (checked on the host)
         const int64_t off = static_cast<int64_t>(t) * kTileElems;
         mbar_arrive_expect_tx(&bars[s], kKPageBytes + kVPageBytes);
         bulk_g2s_evict_first(ring.k[s], k_cache + off, kKPageBytes, &bars[s], policy);
@@ -289,6 +304,13 @@ __global__ void __launch_bounds__(kWarps * 32, kBalCtasPerSm) decode_balanced_ke
       if (ok) {
         if (ring.live[s]) {
           const int valid = min(kPage, cs.L - (fc - cs.s0) * kPage);
+          if constexpr (kAppend) {
+            if (fc - cs.s0 == (cs.L - 1) / kPage) {  // the page of position L - 1
+              const int64_t src = (static_cast<int64_t>(cs.b) * hkv + cs.g) * kHeadDim;
+              append_new_row(ring, s, (cs.L - 1) % kPage, k_new + src, v_new + src,
+                             __ldg(v_scale + cs.g), k_cache, v_cache, ring.live[s] - 1);
+            }
+          }
           attend_page<false>(ring, s, valid, qf, qs, st);
         }
         __syncwarp();
@@ -478,19 +500,22 @@ static int32_t bal_check(int32_t batch, int32_t num_qo_heads, int32_t num_kv_hea
   return K16V8_OK;
 }
 
-extern "C" int32_t k16v8_paged_decode_balanced_split(
-    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
-    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
-    int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-    int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
-    float *lse, int32_t flags, int32_t *dev_error, void *stream) {
+template <bool kAppend>
+static int32_t balanced_split(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                              uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
+                              int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch,
+                              int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t num_pages, float sm_scale, void *workspace,
+                              size_t workspace_bytes, void *out, float *lse, int32_t flags,
+                              int32_t *dev_error, void *stream) {
   BalLayout w;
   int32_t st = bal_check(batch, num_qo_heads, num_kv_heads, head_dim, &w);
   if (st != K16V8_OK) return st;
   if (num_pages <= 0 || max_pages_per_seq < 0) return K16V8_ERR_INVALID_ARG;
   if (flags & ~K16V8_DECODE_METADATA_READY) return K16V8_ERR_INVALID_ARG;
   // Tile indices pid * num_kv_heads + g are int32.
-  if (static_cast<int64_t>(num_pages) * num_kv_heads >= (1LL << 31)) return K16V8_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_pages) * num_kv_heads >= (1LL << 31) - 1)
+    return K16V8_ERR_INVALID_ARG;
   // Flat tile indices are int32: batch * max_pages * num_kv_heads must fit.
   if (static_cast<int64_t>(batch) * max_pages_per_seq * num_kv_heads >= (1LL << 31) - 256 ||
       static_cast<int64_t>(max_pages_per_seq) * kPage >= (1LL << 31))
@@ -503,12 +528,15 @@ extern "C" int32_t k16v8_paged_decode_balanced_split(
       !k16v8_aligned(seq_lens, 4) || !k16v8_aligned(v_scale, 4) || !k16v8_aligned(out, 8) ||
       (lse && !k16v8_aligned(lse, 4)))
     return K16V8_ERR_INVALID_ARG;
+  if (kAppend && (!k_new || !v_new || !k16v8_aligned(k_new, 16) || !k16v8_aligned(v_new, 16)))
+    return K16V8_ERR_INVALID_ARG;
   if (workspace_bytes < w.total) return K16V8_ERR_WORKSPACE_TOO_SMALL;
   static bool configured[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return K16V8_ERR_CUDA;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(decode_balanced_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_balanced_kernel<kAppend>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kBalSmemBytes)) != cudaSuccess)
       return K16V8_ERR_CUDA;
     if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -518,13 +546,39 @@ extern "C" int32_t k16v8_paged_decode_balanced_split(
   if (st != K16V8_OK) return st;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   return k16v8_launch_pdl(
-      decode_balanced_kernel, dim3(ctas), dim3(kWarps * 32), kBalSmemBytes,
+      decode_balanced_kernel<kAppend>, dim3(ctas), dim3(kWarps * 32), kBalSmemBytes,
       static_cast<cudaStream_t>(stream), static_cast<const __half *>(q),
-      static_cast<const __half *>(k_cache), v_cache, v_scale, block_table, max_pages_per_seq,
-      seq_lens, batch, num_qo_heads, num_kv_heads, num_pages, sm_scale,
+      static_cast<__half *>(k_cache), v_cache, v_scale, block_table, max_pages_per_seq, seq_lens,
+      batch, num_qo_heads, num_kv_heads, num_pages, sm_scale,
       reinterpret_cast<int32_t *>(ws + w.plan_off), reinterpret_cast<float *>(ws + w.o_off),
-      reinterpret_cast<float *>(ws + w.lse_off), static_cast<__half *>(out), lse, dev_error,
-      flags);
+      reinterpret_cast<float *>(ws + w.lse_off), static_cast<__half *>(out), lse,
+      static_cast<const __half *>(k_new), static_cast<const __half *>(v_new), dev_error, flags);
+}
+
+extern "C" int32_t k16v8_paged_decode_balanced_split(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
+    float *lse, int32_t flags, int32_t *dev_error, void *stream) {
+  // The kernel only reads the cache when it does not append.
+  return balanced_split<false>(q, nullptr, nullptr, const_cast<void *>(k_cache),
+                               const_cast<uint8_t *>(v_cache), v_scale, block_table,
+                               max_pages_per_seq, seq_lens, batch, num_qo_heads, num_kv_heads,
+                               head_dim, num_pages, sm_scale, workspace, workspace_bytes, out, lse,
+                               flags, dev_error, stream);
+}
+
+extern "C" int32_t k16v8_paged_decode_append_balanced_split(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, uint8_t *v_cache,
+    const float *v_scale, const int32_t *block_table, int32_t max_pages_per_seq,
+    const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes,
+    void *out, float *lse, int32_t flags, int32_t *dev_error, void *stream) {
+  return balanced_split<true>(q, k_new, v_new, k_cache, v_cache, v_scale, block_table,
+                              max_pages_per_seq, seq_lens, batch, num_qo_heads, num_kv_heads,
+                              head_dim, num_pages, sm_scale, workspace, workspace_bytes, out, lse,
+                              flags, dev_error, stream);
 }
 
 extern "C" int32_t k16v8_merge_balanced(const void *workspace, size_t workspace_bytes,
@@ -558,6 +612,21 @@ extern "C" int32_t k16v8_paged_decode_attention_balanced(
     float *lse, int32_t flags, int32_t *dev_error, void *stream) {
   const int32_t st = k16v8_paged_decode_balanced_split(
       q, k_cache, v_cache, v_scale, block_table, max_pages_per_seq, seq_lens, batch,
+      num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale, workspace, workspace_bytes, out,
+      lse, flags, dev_error, stream);
+  if (st != K16V8_OK || batch == 0) return st;
+  return k16v8_merge_balanced(workspace, workspace_bytes, batch, num_qo_heads, num_kv_heads,
+                              head_dim, out, lse, stream);
+}
+
+extern "C" int32_t k16v8_paged_decode_append_attention_balanced(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, uint8_t *v_cache,
+    const float *v_scale, const int32_t *block_table, int32_t max_pages_per_seq,
+    const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes,
+    void *out, float *lse, int32_t flags, int32_t *dev_error, void *stream) {
+  const int32_t st = k16v8_paged_decode_append_balanced_split(
+      q, k_new, v_new, k_cache, v_cache, v_scale, block_table, max_pages_per_seq, seq_lens, batch,
       num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale, workspace, workspace_bytes, out,
       lse, flags, dev_error, stream);
   if (st != K16V8_OK || batch == 0) return st;

@@ -112,6 +112,41 @@ struct WarpState {
   }
 };
 
+// A decode step's new token for one (sequence, KV head): lanes 0-15 each take
+// 8 dims of k_src / v_src (fp16), quantise V as the cache append does (IEEE
+// division by the scale, round to nearest even, saturation), put the row into
+// row `row` of the staged page (slot s) -- the staged copy may predate the
+// store -- and, when tile >= 0, into that cache tile (page id * hkv + head).
+template <typename Ring>
+__device__ __forceinline__ void append_new_row(Ring &ring, int s, int row,
+                                               const __half *__restrict__ k_src,
+                                               const __half *__restrict__ v_src, float scale,
+                                               __half *k_cache, uint8_t *v_cache, int64_t tile) {
+  const int lane = threadIdx.x & 31;
+  if (lane < kHeadDim / 8) {
+    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_src) + lane);
+    const uint4 vraw = __ldg(reinterpret_cast<const uint4 *>(v_src) + lane);
+    const __half2 *vh = reinterpret_cast<const __half2 *>(&vraw);
+    uint32_t w[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float2 a = __half22float2(vh[2 * u]);
+      const float2 c = __half22float2(vh[2 * u + 1]);
+      w[u] = static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale))) |
+             (static_cast<uint32_t>(e4m3x2_from_f32(__fdiv_rn(c.x, scale), __fdiv_rn(c.y, scale)))
+              << 16);
+    }
+    *reinterpret_cast<uint4 *>(ring.k[s] + row * 256 + lane * 16) = kv;
+    *reinterpret_cast<uint2 *>(ring.v[s] + row * kHeadDim + lane * 8) = make_uint2(w[0], w[1]);
+    if (tile >= 0) {
+      const int64_t dst = (tile * kPage + row) * kHeadDim + lane * 8;
+      *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
+      *reinterpret_cast<uint2 *>(v_cache + dst) = make_uint2(w[0], w[1]);
+    }
+  }
+  __syncwarp();
+}
+
 // Fold one staged page (slot s of `ring`, its first `valid` tokens) into the
 // warp's state.  qs = softmax scale * log2(e).
 template <bool kVF16, typename Ring>

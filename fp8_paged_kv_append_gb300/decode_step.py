@@ -41,10 +41,15 @@ class MultiLayerDecode:
     of each sequence goes).
 
     schedule "chunked": split-KV with a fixed split_chunk, then the merge;
+    "fused": the same with each layer's append done by the split kernel;
     "balanced": the load-balanced split (one full wave of equal tile ranges)
-    and its merge.  The block table and lengths are written only by host
-    copies, never by the kernel before the attention, so the balanced split
-    may read them ahead of its wait on that kernel."""
+    and its merge; "balanced_fused": the same with each layer's append done
+    by the split kernel itself (2 launches per layer instead of 3; the slot
+    of the new token is then the one the block table gives for position
+    seq_len - 1, which `slots` must agree with).  The block table and lengths
+    are written only by host copies, never by the kernel before the
+    attention, so the balanced split may read them ahead of its wait on that
+    kernel."""
 
     def __init__(self, k_caches, v_caches, v_scales, block_table, seq_lens, slots, max_seq_len,
                  num_qo_heads, sm_scale=None, split_chunk=512, validate=True,
@@ -62,10 +67,10 @@ class MultiLayerDecode:
         self.d = int(k_caches[0].shape[3])
         self.sm_scale = float(sm_scale if sm_scale is not None else 1.0 / math.sqrt(self.d))
         self.chunk = int(split_chunk)
-        if schedule not in ("chunked", "balanced"):
+        if schedule not in ("chunked", "fused", "balanced", "balanced_fused"):
             raise ValueError(f"unknown schedule {schedule!r}")
         self.schedule = schedule
-        if schedule == "balanced":
+        if schedule in ("balanced", "balanced_fused"):
             n = K.k16v8_decode_balanced_workspace_size(self.batch, self.hq, self.d)
         else:
             n = K.k16v8_decode_workspace_size(self.batch, self.hq, self.d, self.max_seq_len,
@@ -73,13 +78,28 @@ class MultiLayerDecode:
         if n == 0:
             raise ValueError("invalid decode workspace shape")
         self.workspace = torch.empty(n, dtype=torch.uint8, device=dev)
-        if schedule == "chunked":
+        if schedule in ("chunked", "fused"):
             self.partial_o, self.partial_lse = K.workspace_views(
                 self.workspace, self.batch, self.hq, self.d, self.max_seq_len, self.chunk)
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
 
     def layer(self, li, q, k_new, v_new, out, lse=None):
+        if self.schedule == "balanced_fused":
+            K.k16v8_paged_decode_append_balanced_split(
+                q, k_new, v_new, self.k_caches[li], self.v_caches[li], self.v_scales[li],
+                self.block_table, self.seq_lens, self.sm_scale, self.workspace, out, lse,
+                self.dev_error, flags=K.DECODE_METADATA_READY)
+            K.k16v8_merge_balanced(self.workspace, self.hkv, out, lse)
+            return
+        if self.schedule == "fused":
+            K.k16v8_paged_decode_append_split(
+                q, k_new, v_new, self.k_caches[li], self.v_caches[li], self.v_scales[li],
+                self.block_table, self.seq_lens, self.max_seq_len, self.sm_scale, self.chunk,
+                self.workspace, self.dev_error)
+            K.k16v8_merge_states(self.partial_o, self.partial_lse, self.seq_lens, self.chunk,
+                                 out, lse)
+            return
         K.k16v8_kv_append(k_new, v_new, self.slots, self.v_scales[li], self.k_caches[li],
                           self.v_caches[li], self.dev_error)
         if self.schedule == "balanced":

@@ -74,6 +74,13 @@ SIGNATURES = {
                                                  _i32, _i32, _i32, _f32, _P, _sz, _P, _P, _i32,
                                                  _P, _P]),
     "k16v8_merge_balanced": (_i32, [_P, _sz, _i32, _i32, _i32, _i32, _P, _P, _P]),
+    "k16v8_paged_decode_append_balanced_split": (_i32, [_P, _P, _P, _P, _P, _P, _P, _i32, _P,
+                                                        _i32, _i32, _i32, _i32, _i32, _f32, _P,
+                                                        _sz, _P, _P, _i32, _P, _P]),
+    "k16v8_paged_decode_append_attention_balanced": (_i32, [_P, _P, _P, _P, _P, _P, _P, _i32,
+                                                            _P, _i32, _i32, _i32, _i32, _i32,
+                                                            _f32, _P, _sz, _P, _P, _i32, _P,
+                                                            _P]),
     "k16v8_read_device_error": (_i32, [_P, _P, ctypes.POINTER(_i32)]),
     "k16v8_status_string": (ctypes.c_char_p, [_i32]),
 }
@@ -337,6 +344,37 @@ def k16v8_merge_balanced(workspace, num_kv_heads, out, lse=None, stream=None):
         _ptr(workspace), workspace.numel() * workspace.element_size(), B, hq, int(num_kv_heads),
         d, _ptr(out), _ptr(lse), _stream(stream))
     _check("k16v8_merge_balanced", st)
+
+
+def _append_balanced(name, q, k_new, v_new, k_cache, v_cache, v_scale, block_table, seq_lens,
+                     sm_scale, workspace, out, lse, dev_error, stream, flags):
+    B, hq, d = q.shape
+    st = getattr(load_library(), name)(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale),
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, hq, k_cache.shape[1], d,
+        k_cache.shape[0], float(sm_scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), int(flags),
+        _ptr(dev_error), _stream(stream))
+    _check(name, st)
+
+
+def k16v8_paged_decode_append_balanced_split(q, k_new, v_new, k_cache, v_cache, v_scale,
+                                             block_table, seq_lens, sm_scale, workspace, out,
+                                             lse=None, dev_error=None, stream=None, flags=0):
+    """Load-balanced decode split with each sequence's new token (k_new,
+    v_new [B, Hkv, D] fp16) written into the cache by the same kernel."""
+    _append_balanced("k16v8_paged_decode_append_balanced_split", q, k_new, v_new, k_cache,
+                     v_cache, v_scale, block_table, seq_lens, sm_scale, workspace, out, lse,
+                     dev_error, stream, flags)
+
+
+def k16v8_paged_decode_append_attention_balanced(q, k_new, v_new, k_cache, v_cache, v_scale,
+                                                 block_table, seq_lens, sm_scale, workspace, out,
+                                                 lse=None, dev_error=None, stream=None, flags=0):
+    """k16v8_paged_decode_append_balanced_split followed by the merge."""
+    _append_balanced("k16v8_paged_decode_append_attention_balanced", q, k_new, v_new, k_cache,
+                     v_cache, v_scale, block_table, seq_lens, sm_scale, workspace, out, lse,
+                     dev_error, stream, flags)
 
 
 def k16v8_read_device_error(dev_error, stream=None) -> int:

@@ -208,14 +208,15 @@ int32_t k16v8_paged_decode_attention(const void *q, const void *k_cache,
  *                that block_table and seq_lens are not written by the kernel
  *                launched immediately before this call on `stream` (host
  *                copies and earlier kernels are fine).  The attention kernel
- *                then reads them, and plans its work, before it waits for
- *                that kernel to finish (programmatic dependent launch); the
- *                cache, q, the workspace and the outputs are still touched
- *                only after the wait.  Without the flag nothing is read
- *                before the wait.
+ *                then reads them, plans its work and asks L2 to prefetch
+ *                each warp's first cache pages before it waits for that
+ *                kernel to finish (programmatic dependent launch); nothing
+ *                of the cache reaches the SMs, and q, the workspace and the
+ *                outputs are not touched, until after the wait.  Without
+ *                the flag nothing is read before the wait.
  * Other arguments, outputs and device errors as for
  * k16v8_paged_decode_attention.  batch * max_pages_per_seq * num_kv_heads
- * and num_pages * num_kv_heads must stay below 2^31
+ * and num_pages * num_kv_heads must stay below 2^31 - 1
  * (K16V8_ERR_INVALID_ARG otherwise).
  */
 #define K16V8_DECODE_METADATA_READY 0x1
@@ -248,6 +249,37 @@ int32_t k16v8_paged_decode_attention_balanced(
     int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
     int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes, void *out,
     float *lse, int32_t flags, int32_t *dev_error, void *stream);
+
+/*
+ * paged_decode_append_balanced_split / paged_decode_append_attention_balanced
+ * -- the load-balanced decode with the step's cache write folded in:
+ * equivalent to k16v8_kv_append of each sequence's new token at position
+ * seq_lens[b] - 1 (slot block_table[b][(L-1)/16]*16 + (L-1)%16) followed by
+ * k16v8_paged_decode_balanced_split (and, for _attention_balanced,
+ * k16v8_merge_balanced), one kernel fewer per step ("Matched diagnostic
+ * profiles": the candidate writes the compressed cache during decode).
+ *   k_new, v_new  device fp16 [batch][num_kv_heads][head_dim], contiguous,
+ *                 16-B aligned: the K and V of each sequence's new token
+ *                 (read after the dependency wait)
+ *   seq_lens      lengths INCLUDING the new token (L = 0: nothing appended)
+ * Other arguments, flags, outputs and errors as for
+ * k16v8_paged_decode_balanced_split / _attention_balanced; the cache row is
+ * written with the rounding of k16v8_kv_append.  A row whose page id is
+ * rejected is neither written nor attended (K16V8_DEVERR_PAGE).
+ */
+int32_t k16v8_paged_decode_append_balanced_split(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, uint8_t *v_cache,
+    const float *v_scale, const int32_t *block_table, int32_t max_pages_per_seq,
+    const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes,
+    void *out, float *lse, int32_t flags, int32_t *dev_error, void *stream);
+
+int32_t k16v8_paged_decode_append_attention_balanced(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, uint8_t *v_cache,
+    const float *v_scale, const int32_t *block_table, int32_t max_pages_per_seq,
+    const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, void *workspace, size_t workspace_bytes,
+    void *out, float *lse, int32_t flags, int32_t *dev_error, void *stream);
 
 /*
  * paged_decode_append_split / paged_decode_append_attention -- one decode

@@ -31,7 +31,8 @@ def test_reference_arm_prints_contract_line():
     import bench
     w, label, chunk = bench.make_workload("1k")
     assert d["metric"] == bench.METRIC
-    assert d["config"] == bench.config_of(w, label, chunk, bench.replicas_for(w), "balanced")
+    assert d["config"] == bench.config_of(w, label, chunk, bench.replicas_for(w),
+                                          bench.DEFAULT_DECODE)
 
 
 def test_replicas_cover_four_l2():

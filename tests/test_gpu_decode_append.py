@@ -79,3 +79,76 @@ def test_fused_append_equals_separate_append(K):
     K.k16v8_paged_decode_attention(to_dev(w.q), kc2, vc2, *args, ws, o2)
     assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16)) and torch.equal(vc, vc2)
     assert torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("maker,flags", [
+    (lambda: workloads.make_decode("ragged with empty", 52, [1, 0, 16, 17, 200, 0, 513, 1000],
+                                   num_qo_heads=8, num_kv_heads=2), 0),
+    (workloads.decode_1k_b32, 1),
+    (workloads.decode_8k_b16, 1)])
+def test_fused_append_balanced_matches_oracle(K, maker, flags):
+    """The load-balanced split with the append folded in: cache bytes equal
+    the oracle's append (whole pool, bit-exact), outputs its decode."""
+    w = maker()
+    w.v_tok = w.v_tok.astype(np.float16)
+    kc, vc, okc, ovc = cache_without_new_tokens(w, K)
+    B, hq, d = w.q.shape
+    has_new = w.new_rows >= 0
+    nr = np.where(has_new, w.new_rows, 0)  # rows of empty sequences are never read
+    ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d), dtype=torch.uint8,
+                     device=dev())
+    out = torch.full((B, hq, d), float("nan"), dtype=torch.float16, device=dev())
+    lse = torch.empty((B, hq), dtype=torch.float32, device=dev())
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    k_new = np.ascontiguousarray(w.k_tok[nr])
+    v_new = np.ascontiguousarray(w.v_tok[nr])
+    K.k16v8_paged_decode_append_attention_balanced(
+        to_dev(w.q), to_dev(k_new), to_dev(v_new), kc, vc, to_dev(w.v_scale),
+        to_dev(w.block_table), to_dev(w.seq_lens), w.sm_scale, ws, out, lse, err, flags=flags)
+    assert K.k16v8_read_device_error(err) == 0
+    sel = w.new_rows[has_new]
+    oracle.kv_append(w.k_tok[sel], w.v_tok[sel], w.slot_mapping[sel], w.v_scale, okc, ovc)
+    hk, hv = host_bits(kc, vc)
+    assert np.array_equal(hk, okc.view(np.uint16)) and np.array_equal(hv, ovc)
+    ref = oracle.paged_decode(w.q, okc, ovc, w.v_scale, w.block_table, w.seq_lens, w.sm_scale)
+    check_close(out.float().cpu().numpy(), ref["out"], lse.cpu().numpy(), ref["lse"])
+
+
+def test_fused_append_balanced_equals_separate_append(K):
+    """Same cache bytes and bit-identical outputs as kv_append followed by
+    the load-balanced decode."""
+    w = workloads.decode_1k_b32(8)
+    kc, vc, _, _ = cache_without_new_tokens(w, K)
+    kc2, vc2 = kc.clone(), vc.clone()
+    B, hq, d = w.q.shape
+    nr = w.new_rows
+    ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d), dtype=torch.uint8,
+                     device=dev())
+    o1 = torch.empty((B, hq, d), dtype=torch.float16, device=dev())
+    o2 = torch.empty_like(o1)
+    l1 = torch.empty((B, hq), dtype=torch.float32, device=dev())
+    l2 = torch.empty_like(l1)
+    args = (to_dev(w.v_scale), to_dev(w.block_table), to_dev(w.seq_lens), w.sm_scale, ws)
+    K.k16v8_paged_decode_append_attention_balanced(
+        to_dev(w.q), to_dev(w.k_tok[nr]), to_dev(w.v_tok[nr].astype(np.float16)), kc, vc, *args,
+        o1, l1)
+    K.k16v8_kv_append(to_dev(w.k_tok[nr]), to_dev(w.v_tok[nr].astype(np.float16)),
+                      to_dev(w.slot_mapping[nr]), to_dev(w.v_scale), kc2, vc2)
+    K.k16v8_paged_decode_attention_balanced(to_dev(w.q), kc2, vc2, *args, o2, l2)
+    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16)) and torch.equal(vc, vc2)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+def test_fused_append_balanced_host_checks(K):
+    w = workloads.tiny_decode(0)
+    B, hq, d = w.q.shape
+    kc, vc = gpu_poisoned_caches(w.num_pages, w.num_kv_heads, w.head_dim)
+    ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d), dtype=torch.uint8,
+                     device=dev())
+    out = torch.empty((B, hq, d), dtype=torch.float16, device=dev())
+    kn = torch.zeros((B, w.num_kv_heads, d), dtype=torch.float16, device=dev())
+    with pytest.raises(K.K16V8Error) as e:  # v_new missing
+        K.k16v8_paged_decode_append_balanced_split(
+            to_dev(w.q), kn, None, kc, vc, to_dev(w.v_scale), to_dev(w.block_table),
+            to_dev(w.seq_lens), w.sm_scale, ws, out)
+    assert e.value.status == K.K16V8_ERR_INVALID_ARG
