@@ -358,12 +358,15 @@ class DecodeBench:
         return np.array([outs])
 
     def run_e2e(self, steps, warmup):
-        """Same steps through host buffers: each step copies its inputs (q,
+        """Same steps through host buffers.  Every step copies its inputs (q,
         the new K/V rows, lengths, block table, slots) from one pinned host
-        buffer to the device, runs the launches, and reads out + lse back
-        into one pinned host buffer -- one copy each way, all inside the
-        timed region (host wall clock).  The steps are captured back to back
-        in one CUDA graph; its memcpy nodes still move the bytes every step."""
+        buffer to the device in one copy, runs the launches, and reads out +
+        lse back into a pinned host buffer in one copy, all inside the timed
+        region (host wall clock).  The copies are pipelined as a serving loop
+        would: step i+1's inputs go up (copy stream) and step i-1's results
+        come down (a second copy stream) while step i computes, with two
+        device buffers each way; every step still moves all of its bytes.
+        The steps are captured back to back in one CUDA graph."""
         torch, K, w = self.torch, self.K, self.w
         align = lambda n: (n + 255) // 256 * 256
         parts = [("q", self.q), ("k_new", self.k_new), ("v_new", self.v_new),
@@ -381,49 +384,93 @@ class DecodeBench:
                 buf[offs[name]:offs[name] + nb].copy_(src.cpu().contiguous().view(-1)
                                                       .view(torch.uint8))
             h_in.append(buf)
-        d_in = torch.empty(total, dtype=torch.uint8, device=self.dev)
-        view = lambda name, t: d_in[offs[name]:offs[name] + t.numel() * t.element_size()] \
-            .view(t.dtype).view(t.shape)
-        d = {name: view(name, t) for name, t in parts}
         o_bytes = self.out.numel() * 2
-        d_out = torch.empty(align(o_bytes) + self.lse.numel() * 4, dtype=torch.uint8,
-                            device=self.dev)
-        out = d_out[:o_bytes].view(torch.float16).view(self.out.shape)
-        lse = d_out[align(o_bytes):].view(torch.float32).view(self.lse.shape)
-        h_out = torch.empty(d_out.numel(), dtype=torch.uint8).pin_memory()
+        out_total = align(o_bytes) + self.lse.numel() * 4
+        d_in = [torch.empty(total, dtype=torch.uint8, device=self.dev) for _ in range(2)]
+        d_out = [torch.empty(out_total, dtype=torch.uint8, device=self.dev) for _ in range(2)]
+        h_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+
+        def views(k):
+            v = lambda name, t: d_in[k][offs[name]:offs[name] + t.numel() * t.element_size()] \
+                .view(t.dtype).view(t.shape)
+            d = {name: v(name, t) for name, t in parts}
+            d["out"] = d_out[k][:o_bytes].view(torch.float16).view(self.out.shape)
+            d["lse"] = d_out[k][align(o_bytes):].view(torch.float32).view(self.lse.shape)
+            return d
+
+        dv = [views(0), views(1)]
         h2d = sum(t.numel() * t.element_size() for _, t in parts)
         d2h = o_bytes + self.lse.numel() * 4
 
-        def one(i):
-            d_in.copy_(h_in[i % self.R], non_blocking=True)
+        def compute(d):
             if self.mode == "balanced_fused":
                 K.k16v8_paged_decode_append_attention_balanced(
                     d["q"], d["k_new"], d["v_new"], self.kc, self.vc, self.v_scale, d["bt"],
-                    d["seq_lens"], w.sm_scale, self.ws, out, lse, self.err,
+                    d["seq_lens"], w.sm_scale, self.ws, d["out"], d["lse"], self.err,
                     flags=K.DECODE_METADATA_READY)
-                h_out.copy_(d_out, non_blocking=True)
+                return
+            if self.mode == "fused":
+                K.k16v8_paged_decode_append_attention(
+                    d["q"], d["k_new"], d["v_new"], self.kc, self.vc, self.v_scale, d["bt"],
+                    d["seq_lens"], self.max_len, w.sm_scale, self.chunk, self.ws, d["out"],
+                    d["lse"], self.err)
                 return
             K.k16v8_kv_append(d["k_new"], d["v_new"], d["slots"], self.v_scale, self.kc,
                               self.vc, self.err)
             if self.mode == "balanced":
-                K.k16v8_paged_decode_attention_balanced(d["q"], self.kc, self.vc,
-                                                        self.v_scale, d["bt"], d["seq_lens"],
-                                                        w.sm_scale, self.ws, out, lse,
-                                                        self.err, flags=K.DECODE_METADATA_READY)
+                K.k16v8_paged_decode_attention_balanced(d["q"], self.kc, self.vc, self.v_scale,
+                                                        d["bt"], d["seq_lens"], w.sm_scale,
+                                                        self.ws, d["out"], d["lse"], self.err,
+                                                        flags=K.DECODE_METADATA_READY)
             else:
                 K.k16v8_paged_decode_attention(d["q"], self.kc, self.vc, self.v_scale, d["bt"],
                                                d["seq_lens"], self.max_len, w.sm_scale,
-                                               self.chunk, self.ws, out, lse, self.err)
-            h_out.copy_(d_out, non_blocking=True)
+                                               self.chunk, self.ws, d["out"], d["lse"],
+                                               self.err)
 
-        for i in range(warmup):
-            one(i)
+        up = torch.cuda.Stream(self.dev)
+        down = torch.cuda.Stream(self.dev)
+
+        def run(n, first):
+            """n pipelined steps on the current stream (step indices first..)."""
+            main = torch.cuda.current_stream(self.dev)
+            ev = lambda: torch.cuda.Event()
+            in_ready, done, read = [None] * n, [None] * n, [None] * n
+            up.wait_stream(main)
+            down.wait_stream(main)
+            with torch.cuda.stream(up):
+                d_in[0].copy_(h_in[first % self.R], non_blocking=True)
+                in_ready[0] = ev()
+                in_ready[0].record(up)
+            for i in range(n):
+                k = i % 2
+                if i + 1 < n:  # next step's inputs into the other buffer
+                    with torch.cuda.stream(up):
+                        if i >= 1:
+                            up.wait_event(done[i - 1])  # step i-1 has read that buffer
+                        d_in[1 - k].copy_(h_in[(first + i + 1) % self.R], non_blocking=True)
+                        in_ready[i + 1] = ev()
+                        in_ready[i + 1].record(up)
+                main.wait_event(in_ready[i])
+                if i >= 2:
+                    main.wait_event(read[i - 2])  # its output buffer has been read back
+                compute(dv[k])
+                done[i] = ev()
+                done[i].record(main)
+                with torch.cuda.stream(down):
+                    down.wait_event(done[i])
+                    h_out[k].copy_(d_out[k], non_blocking=True)
+                    read[i] = ev()
+                    read[i].record(down)
+            main.wait_stream(up)
+            main.wait_stream(down)
+
+        run(max(warmup, 2), 0)
         torch.cuda.synchronize(self.dev)
         side = torch.cuda.Stream(self.dev)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
-            for i in range(steps):
-                one(i)
+            run(steps, 0)
         graph.replay()
         torch.cuda.synchronize(self.dev)
         barrier()
@@ -432,8 +479,12 @@ class DecodeBench:
         torch.cuda.synchronize(self.dev)
         dt = (time.perf_counter() - t0) * 1e3 / steps
         barrier()
-        if not (torch.equal(out, self.out) or self.mode == "fused"):
+        last = dv[(steps - 1) % 2]
+        if not torch.equal(last["out"], self.out):
             raise RuntimeError("end-to-end step disagrees with the device-resident step")
+        host = h_out[(steps - 1) % 2][:o_bytes].view(torch.float16).view(self.out.shape)
+        if not torch.equal(host, self.out.cpu()):
+            raise RuntimeError("end-to-end result read back to the host disagrees")
         return dt, h2d, d2h
 
 

@@ -43,6 +43,7 @@ constexpr int kBalCtasPerSm = kMinBlocks;
 constexpr int kBalMinTiles = kWarps;  // at least one tile per warp
 constexpr int kBalMaxBatch = 8192;    // the scan's page offsets live in the ring space
 constexpr int kPrefetchTiles = 2;      // per warp, into L2 before the dependency wait
+constexpr int kMergeFast = 8;          // cut pieces merged from one round of loads
 
 // Cross-warp combine staging (warps 1..3) plus a few scalars.
 struct BalStage {
@@ -437,19 +438,52 @@ __global__ void __launch_bounds__(128, 8) merge_balanced_kernel(
     auto row_of = [&](int c) {  // partial row of the c-th cutting CTA
       return (static_cast<int64_t>(i0 + c) * 2 + (c == 0 ? slot0 : 0)) * kGroup + hh;
     };
-    for (int c = lane; c < n; c += 32) M = fmaxf(M, __ldg(part_lse + row_of(c)));
+    if (n <= kMergeFast) {
+      // Every partial of the segment in one round of loads (the common
+      // case: a segment is cut by a few CTAs), then the same sums in the
+      // same order as the general loop below.
+      const float lc = lane < n ? __ldg(part_lse + row_of(lane)) : -INFINITY;
+      float4 oc[kMergeFast];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    if (M != -INFINITY) {
-      for (int c = 0; c < n; ++c) {
-        const int64_t r = row_of(c);
-        const float4 oc = __ldg(reinterpret_cast<const float4 *>(part_o + r * kHeadDim + lane * 4));
-        const float wu = ex2((__ldg(part_lse + r) - M) * kLog2e);
-        S += wu;
-        acc.x = fmaf(wu, oc.x, acc.x);
-        acc.y = fmaf(wu, oc.y, acc.y);
-        acc.z = fmaf(wu, oc.z, acc.z);
-        acc.w = fmaf(wu, oc.w, acc.w);
+      for (int c = 0; c < kMergeFast; ++c)
+        oc[c] = c < n ? __ldg(reinterpret_cast<const float4 *>(part_o + row_of(c) * kHeadDim +
+                                                               lane * 4))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      float lw[kMergeFast];
+#pragma unroll
+      for (int c = 0; c < kMergeFast; ++c) {
+        lw[c] = __shfl_sync(kFull, lc, c);
+        M = fmaxf(M, lw[c]);
+      }
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int c = 0; c < kMergeFast; ++c) {
+          if (c < n) {
+            const float wu = ex2((lw[c] - M) * kLog2e);
+            S += wu;
+            acc.x = fmaf(wu, oc[c].x, acc.x);
+            acc.y = fmaf(wu, oc[c].y, acc.y);
+            acc.z = fmaf(wu, oc[c].z, acc.z);
+            acc.w = fmaf(wu, oc[c].w, acc.w);
+          }
+        }
+      }
+    } else {
+      for (int c = lane; c < n; c += 32) M = fmaxf(M, __ldg(part_lse + row_of(c)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+      if (M != -INFINITY) {
+        for (int c = 0; c < n; ++c) {
+          const int64_t r = row_of(c);
+          const float4 oc =
+              __ldg(reinterpret_cast<const float4 *>(part_o + r * kHeadDim + lane * 4));
+          const float wu = ex2((__ldg(part_lse + r) - M) * kLog2e);
+          S += wu;
+          acc.x = fmaf(wu, oc.x, acc.x);
+          acc.y = fmaf(wu, oc.y, acc.y);
+          acc.z = fmaf(wu, oc.z, acc.z);
+          acc.w = fmaf(wu, oc.w, acc.w);
+        }
       }
     }
   }
