@@ -676,6 +676,7 @@ def fullpool_line(device, steps, warmup, hbm_peak, layers=40, schedule="chunked"
     step = MultiLayerDecode([p[0] for p in pools], [p[1] for p in pools], [p[2] for p in pools],
                             td(lay.block_table), td(lay.seq_lens), td(slots), int(L.max()), 40,
                             split_chunk=512, schedule=schedule)
+    chosen = step.schedule
     outs = [torch.empty((B, 40, 128), dtype=torch.float16, device=device) for _ in range(layers)]
     lses = [torch.empty((B, 40), dtype=torch.float32, device=device) for _ in range(layers)]
     step.capture(qs, kn, vn, outs, lses)
@@ -701,11 +702,12 @@ def fullpool_line(device, steps, warmup, hbm_peak, layers=40, schedule="chunked"
                         + {"chunked": "split 512", "fused": "split 512 with the append folded in",
                            "balanced": "load-balanced split",
                            "balanced_fused": "load-balanced split with the append folded in"}
-                        [schedule] + ", one CUDA graph per step",
+                        [chosen] + (" (chosen by the tiles-per-CTA rule)" if schedule == "auto"
+                                    else "") + ", one CUDA graph per step",
             "ms_per_step": round(ms, 4), "us_per_layer_step": round(ms * 1e3 / layers, 2),
             "kv_bytes_per_step": kvb, "value": round(kvb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
-            "gpu_launches_per_step": (2 if schedule in ("fused", "balanced_fused") else 3) * layers}
+            "gpu_launches_per_step": (2 if chosen in ("fused", "balanced_fused") else 3) * layers}
 
 
 # ---- CPU baseline: the oracle on the host cores -------------------------------------
@@ -921,11 +923,10 @@ def main():
             line["extra"][f"{name}_fp16_kv_control"] = ctl
         torch.cuda.empty_cache()
         line["extra"]["fullpool_40_layers"] = fullpool_line(device, 10, 3, hbm_peak,
-                                                            schedule=args.decode)
+                                                            schedule="auto")
         for m in MODES:
-            if m != args.decode:
-                line["extra"][f"fullpool_40_layers_{SUFFIX[m]}"] = fullpool_line(
-                    device, 10, 3, hbm_peak, schedule=m)
+            line["extra"][f"fullpool_40_layers_{SUFFIX[m]}"] = fullpool_line(
+                device, 10, 3, hbm_peak, schedule=m)
         _, tpeak, tkind = load_peaks()
         torch.cuda.empty_cache()
         line["extra"]["prefill"] = {

@@ -32,6 +32,26 @@ def validate_scales(v_scales) -> None:
             raise ScaleError(f"layer {li}: value scale not finite and positive at KV heads {idx}")
 
 
+# Tiles per CTA of the load-balanced split (one full wave of SMs x 4 CTAs)
+# above which the chunked split takes over.  Measured on GB300 (per
+# layer-step, append folded in): 37 tiles per CTA (decode 1K/b32) balanced
+# 26.1 us against chunked 29.1 us; 136 (8K/b16) 80.7 against 81.6 us; 225
+# (64 ragged sequences over a 32 GiB pool) 138.5 against 126.3 us.  The
+# balanced split removes the chunked split's partial last wave, which costs
+# most when there are few waves; with long ranges per CTA the CTAs of one SM
+# drift apart and the chunked split's many short CTAs even out better.
+BALANCED_MAX_TILES_PER_CTA = 160
+
+
+def choose_schedule(seq_lens_host, num_kv_heads: int, num_sms: int) -> str:
+    """"balanced_fused" or "fused" (both with the append folded in) for a
+    batch with these lengths, by the rule above."""
+    pages = sum((int(L) + 15) // 16 for L in seq_lens_host if int(L) > 0)
+    tiles = pages * int(num_kv_heads)
+    per_cta = -(-tiles // (int(num_sms) * 4)) if tiles else 0
+    return "balanced_fused" if per_cta <= BALANCED_MAX_TILES_PER_CTA else "fused"
+
+
 class MultiLayerDecode:
     """Decode step over `len(k_caches)` layers that share one page table.
 
@@ -49,7 +69,8 @@ class MultiLayerDecode:
     seq_len - 1, which `slots` must agree with).  The block table and lengths
     are written only by host copies, never by the kernel before the
     attention, so the balanced split may read them ahead of its wait on that
-    kernel."""
+    kernel.  "auto" picks "balanced_fused" or "fused" by choose_schedule
+    from the lengths (copied to the host once, at construction)."""
 
     def __init__(self, k_caches, v_caches, v_scales, block_table, seq_lens, slots, max_seq_len,
                  num_qo_heads, sm_scale=None, split_chunk=512, validate=True,
@@ -67,6 +88,9 @@ class MultiLayerDecode:
         self.d = int(k_caches[0].shape[3])
         self.sm_scale = float(sm_scale if sm_scale is not None else 1.0 / math.sqrt(self.d))
         self.chunk = int(split_chunk)
+        if schedule == "auto":  # by the lengths of this batch (read once, here)
+            schedule = choose_schedule(seq_lens.detach().cpu().tolist(), k_caches[0].shape[1],
+                                       torch.cuda.get_device_properties(dev).multi_processor_count)
         if schedule not in ("chunked", "fused", "balanced", "balanced_fused"):
             raise ValueError(f"unknown schedule {schedule!r}")
         self.schedule = schedule

@@ -103,17 +103,23 @@ def test_scale_validation_rejects_bad_scale(setup):
         validate_scales(bad)
 
 
-def test_fullpool_balanced_schedule_matches_oracle(setup):
-    """The same 40-layer step on the load-balanced split (captured graph, block
-    table and lengths read ahead of the wait on the append kernel): sampled
-    (layer, sequence) pairs against the oracle."""
+@pytest.mark.parametrize("schedule", ["balanced", "balanced_fused", "fused", "auto"])
+def test_fullpool_other_schedules_match_oracle(setup, schedule):
+    """The same 40-layer step on the load-balanced split (block table and
+    lengths read ahead of the wait on the preceding kernel), with and without
+    the append folded in, the chunked split with the append folded in, and
+    the automatic choice (captured graph each): sampled (layer, sequence)
+    pairs against the oracle.  Folded-in appends write the same bytes to the
+    same slots as the separate append."""
     from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
     s = setup
     lay, B = s["lay"], len(s["lay"].seq_lens)
     step = MultiLayerDecode([p[0] for p in s["pools"]], [p[1] for p in s["pools"]],
                             [p[2] for p in s["pools"]], to_dev(lay.block_table),
                             to_dev(lay.seq_lens), to_dev(s["slots"]),
-                            int(lay.seq_lens.max()), 40, schedule="balanced")
+                            int(lay.seq_lens.max()), 40, schedule=schedule)
+    if schedule == "auto":
+        assert step.schedule == "fused"  # 225 tiles per CTA on 152 SMs
     outs = [torch.full((B, 40, 128), float("nan"), dtype=torch.float16, device=dev())
             for _ in range(LAYERS)]
     lses = [torch.full((B, 40), float("nan"), dtype=torch.float32, device=dev())
