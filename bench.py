@@ -569,10 +569,13 @@ class PrefillBench:
     """All calls of a chunked-prefill workload (per call: kv_append of the
     chunk, then prefill attention), replayed from CUDA graphs."""
 
-    def __init__(self, p, device):
+    def __init__(self, p, device, split=True):
+        """split: the KV-split call (parts chosen by the library; one
+        zero-filled workspace for all calls) instead of the plain call."""
         import torch
         from fp8_paged_kv_append_gb300 import k16v8 as K
         self.K, self.torch, self.p, self.dev = K, torch, p, device
+        self.split = split
         td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
         self.kc = torch.zeros((p.num_pages, p.num_kv_heads, 16, p.head_dim), dtype=torch.float16,
                               device=device)
@@ -590,14 +593,24 @@ class PrefillBench:
                 out=torch.empty(q.shape, dtype=torch.float16, device=device),
                 lse=torch.empty(q.shape[:2], dtype=torch.float32, device=device)))
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        n = max(K.k16v8_prefill_workspace_size(c["max_qlen"], len(pc.seq_lens), p.num_qo_heads,
+                                               p.num_kv_heads, p.head_dim, 0)
+                for c, pc in zip(self.calls, p.calls))
+        self.ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+        self.ws_bytes = n
 
     def append(self, c):
         self.K.k16v8_kv_append(c["k"], c["v"], c["slots"], self.vs, self.kc, self.vc, self.err)
 
     def attend(self, c):
-        self.K.k16v8_paged_prefill_attention(c["q"], c["indptr"], c["max_qlen"], self.kc, self.vc,
-                                             self.vs, c["bt"], c["lens"], self.p.sm_scale,
-                                             c["out"], c["lse"], self.err)
+        if self.split:
+            self.K.k16v8_paged_prefill_attention_split(
+                c["q"], c["indptr"], c["max_qlen"], self.kc, self.vc, self.vs, c["bt"], c["lens"],
+                self.p.sm_scale, self.ws, c["out"], c["lse"], self.err)
+        else:
+            self.K.k16v8_paged_prefill_attention(c["q"], c["indptr"], c["max_qlen"], self.kc,
+                                                 self.vc, self.vs, c["bt"], c["lens"],
+                                                 self.p.sm_scale, c["out"], c["lse"], self.err)
 
     def step(self):
         for c in self.calls:
@@ -639,15 +652,26 @@ class PrefillBench:
 
 
 def prefill_line(p, device, steps, warmup, tensor_peak):
-    pb = PrefillBench(p, device)
+    """The prefill calls through the KV-split entry point (the library picks
+    the parts; 1 when the items fill the GPU), and the plain call beside it
+    when the split one split anything."""
+    pb = PrefillBench(p, device, split=True)
     step_ms, attn_ms, app_ms = pb.run(steps, warmup)
     fl = prefill_flops(p)
-    return {"workload": p.name, "calls": len(p.calls), "query_tokens": int(p.q.shape[0]),
+    line = {"workload": p.name, "calls": len(p.calls), "query_tokens": int(p.q.shape[0]),
             "ms_per_prompt_batch": round(step_ms, 4),
             "prefill_attention_ms": round(attn_ms, 4), "kv_append_ms": round(app_ms, 4),
             "algorithmic_tflop": round(fl / 1e12, 4),
             "prefill_tflops": round(fl / (attn_ms * 1e-3) / 1e12, 1),
-            "frac_of_fp16_tensor_peak": round(fl / (attn_ms * 1e-3) / 1e12 / tensor_peak, 4)}
+            "frac_of_fp16_tensor_peak": round(fl / (attn_ms * 1e-3) / 1e12 / tensor_peak, 4),
+            "kv_split_workspace_bytes": pb.ws_bytes}
+    if pb.ws_bytes:
+        del pb
+        plain = PrefillBench(p, device, split=False)
+        _, attn0, _ = plain.run(steps, warmup)
+        line["unsplit_prefill_attention_ms"] = round(attn0, 4)
+        line["unsplit_prefill_tflops"] = round(fl / (attn0 * 1e-3) / 1e12, 1)
+    return line
 
 
 # ---- full-pool ragged decode across 40 layers ------------------------------------

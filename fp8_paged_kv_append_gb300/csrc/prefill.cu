@@ -34,6 +34,9 @@
 // wait is bounded.
 #include <math.h>
 
+#include <algorithm>
+#include <cmath>
+
 #include <cudaTypedefs.h>
 
 #include "k16v8_device.cuh"
@@ -64,6 +67,8 @@ constexpr uint32_t kOffIds = kOffV + 2 * kVStage;
 constexpr uint32_t kOffBar = kOffIds + kMaxIdPages * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256;
 constexpr uint32_t kTmemCols = 512;  // S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512)
+constexpr int kMaxKvParts = 4;       // KV split of one work item, at most
+constexpr int kMinPartTiles = 8;     // KV tiles per part, at least
 
 enum {
   kBarQ = 0,
@@ -111,6 +116,10 @@ __device__ __forceinline__ bool wait_all3(uint64_t *a, uint32_t pa, uint64_t *b,
   return false;
 }
 
+// kSplit: the KV-split form (parts of a pair's KV range, merged by the last
+// part); the plain form is compiled without any of that code, which keeps
+// its instruction footprint as small as it was.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_o,
@@ -118,7 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const int32_t *__restrict__ qo_indptr, const int32_t *__restrict__ block_table, int32_t maxp,
     const int32_t *__restrict__ seq_lens, int32_t total_q, int32_t hq, int32_t hkv,
     int32_t num_pages, float sm_scale, __half *__restrict__ out, float *__restrict__ lse_out,
-    int32_t *dev_error) {
+    int32_t *dev_error, int32_t kv_parts, uint4 *__restrict__ part_o,
+    float *__restrict__ part_lse, int32_t *__restrict__ counters) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *base = smem_raw;
   uint8_t *sQ = base + kOffQ;
@@ -129,10 +139,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kOffBar + kNumBars * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kOffBar + kNumBars * 8 + 4);
+  volatile int *last_flag = reinterpret_cast<volatile int *>(base + kOffBar + kNumBars * 8 + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y, b = blockIdx.z;
-  const int pair = gridDim.x - 1 - blockIdx.x;  // longest (latest) tiles first
+  const int parts = kSplit ? kv_parts : 1;
+  const int max_pairs = gridDim.x / parts;
+  const int slot = blockIdx.x / parts, part = blockIdx.x - slot * parts;
+  const int pair = max_pairs - 1 - slot;  // longest (latest) tiles first
   pdl_wait();
   if (smem_addr(smem_raw) & 1023u) {  // operand tiles need 1024-byte alignment
     if (tid == 0) flag_error(dev_error, K16V8_DEVERR_INTERNAL);
@@ -150,8 +164,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   if (t_lo >= qlen) return;
   const int pos0 = L - qlen;          // absolute position of new token 0
   const int p_hi = pos0 + min(t_lo + 2 * kQTok, qlen) - 1;  // last position of the pair
-  const int n_kv = p_hi / kKv + 1;
-  const int32_t *bt = block_table + static_cast<int64_t>(b) * maxp;
+  const int n_all = p_hi / kKv + 1;  // KV tiles of the pair
+  // KV split: part `part` of `live_parts` takes tiles [kv0, kv0 + n_kv); the
+  // last part to finish merges the parts' rows (see the epilogue)
+  const int live_parts = kSplit ? max(1, min(parts, n_all / kMinPartTiles)) : 1;
+  if (part >= live_parts) return;
+  const bool split = kSplit && live_parts > 1;
+  const int kv0 = part * n_all / live_parts;
+  const int n_kv = (part + 1) * n_all / live_parts - kv0;
+  const int32_t *bt = block_table + static_cast<int64_t>(b) * maxp + kv0 * kPagesPerTile;
 
   if (warp == kLoadWarp && lane == 0) {
     // The query load depends on nothing else: start it before the rest of
@@ -171,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   if (warp == kLoadWarp) {
     // this pair's page ids into shared memory (lane-parallel), overlapping
     // the tensor-memory and barrier set-up of the other warps
-    const int n_ids = min(n_kv * kPagesPerTile, (L + kPage - 1) / kPage);
+    const int n_ids = min(n_kv * kPagesPerTile, (L + kPage - 1) / kPage - kv0 * kPagesPerTile);
     for (int i = lane; i < min(n_ids, kMaxIdPages); i += 32) {
       const int p = __ldg(bt + i);
       page_ids[i] = (p >= 0 && p < num_pages) ? p : -1;
@@ -215,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     for (int j = 0; j < n_kv; ++j) {
       cta_wait(&bars[kBarSFull + w], j & 1, abort_flag, dev_error);
       tc::fence_after_sync();
-      const bool need_mask = j * kKv + kKv - 1 > p_lo;  // diagonal tile
-      const int lim = p_r - j * kKv;  // last visible column of this tile
+      const bool need_mask = (kv0 + j) * kKv + kKv - 1 > p_lo;  // diagonal tile
+      const int lim = p_r - (kv0 + j) * kKv;  // last visible column of this tile
       // pass 1: row max (64 columns per load round)
       float rmax = -INFINITY;
 #pragma unroll
@@ -305,41 +326,146 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const bool full_tile = t_lo + (w + 1) * kQTok <= qlen;  // uniform over the group
     uint8_t *stage = sQ + w * kQBytes;
     const bool o_ready = cta_wait(&bars[kBarODone + w], (n_kv - 1) & 1, abort_flag, dev_error);
-    if (o_ready) {
-      tc::fence_after_sync();
-      const float inv = __ldg(v_scale + g) / l;
-      const int64_t orow = static_cast<int64_t>(q0 + t_abs) * hq + g * kGroup + (r & 3);
+    bool write_out = true;
+    if constexpr (!kSplit) {
+      if (o_ready) {
+        tc::fence_after_sync();
+        const float inv = __ldg(v_scale + g) / l;
+        const int64_t orow = static_cast<int64_t>(q0 + t_abs) * hq + g * kGroup + (r & 3);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tc::tmem_ld32(tO + lane_base + c * 32, o);
-        tc::tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(tO + lane_base + c * 32, o);
+          tc::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t pk[4];
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2 hh = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
-                                                 __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
-            pk[e] = *reinterpret_cast<const uint32_t *>(&hh);
-          }
-          if (full_tile) {
-            // dims 32c + 8q .. +7: box half c >> 1, 16-byte chunk (c & 1) * 4 + q of row r
-            const uint32_t off = static_cast<uint32_t>(r) * 128 + ((c & 1) * 4 + q) * 16;
-            *reinterpret_cast<uint4 *>(stage + (c >> 1) * (kQBytes / 2) + tc::sw128(off)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          } else if (row_valid) {
-            *reinterpret_cast<uint4 *>(out + orow * kHeadDim + c * 32 + q * 8) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int e = 0; e < 4; ++e) {
+              const __half2 hh = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
+                                                   __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
+              pk[e] = *reinterpret_cast<const uint32_t *>(&hh);
+            }
+            if (full_tile) {
+              // dims 32c + 8q .. +7: box half c >> 1, 16-byte chunk (c & 1) * 4 + q of row r
+              const uint32_t off = static_cast<uint32_t>(r) * 128 + ((c & 1) * 4 + q) * 16;
+              *reinterpret_cast<uint4 *>(stage + (c >> 1) * (kQBytes / 2) + tc::sw128(off)) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            } else if (row_valid) {
+              *reinterpret_cast<uint4 *>(out + orow * kHeadDim + c * 32 + q * 8) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
           }
         }
+        if (row_valid && lse_out) lse_out[orow] = (m_used + lg2(l)) * kLn2;
       }
-      if (row_valid && lse_out) lse_out[orow] = (m_used + lg2(l)) * kLn2;
+    } else {
+      const int64_t orow = static_cast<int64_t>(q0 + t_abs) * hq + g * kGroup + (r & 3);
+      auto put = [&](int c16, const uint32_t (&pk)[4]) {  // 8 output dims [8*c16, 8*c16+8)
+        if (full_tile) {
+          // box half c16 >> 3, 16-byte chunk c16 & 7 of row r
+          const uint32_t off = static_cast<uint32_t>(r) * 128 + (c16 & 7) * 16;
+          *reinterpret_cast<uint4 *>(stage + (c16 >> 3) * (kQBytes / 2) + tc::sw128(off)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        } else if (row_valid) {
+          *reinterpret_cast<uint4 *>(out + orow * kHeadDim + c16 * 8) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      };
+      // KV split: every part writes its rows normalised by its own sum (fp16)
+      // and its LSE; the part that finishes last (per-item counter) combines
+      // them -- o = sum_p e^(lse_p - lse) o_p, lse = log sum_p e^lse_p -- and
+      // writes the output.  No part waits for another.
+      const int64_t item = (static_cast<int64_t>(b) * hkv + g) * max_pairs + pair;
+      auto part_base = [&](int q) { return ((item * kv_parts + q) * 2 + w) * kRows; };
+      if (o_ready) {
+        tc::fence_after_sync();
+        const float vs = __ldg(v_scale + g);
+        const float inv = split ? (l > 0.f ? vs / l : 0.f) : vs / l;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(tO + lane_base + c * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half2 hh = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
+                                                   __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
+              pk[e] = *reinterpret_cast<const uint32_t *>(&hh);
+            }
+            if (split)  // [chunk][row] so a warp's 32 rows are one 512-byte run
+              part_o[(part_base(part) / kRows * 16 + c * 4 + q) * kRows + r] =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            else
+              put(c * 4 + q, pk);
+          }
+        }
+        const float lse_row = l > 0.f ? (m_used + lg2(l)) * kLn2 : -INFINITY;
+        if (split)
+          part_lse[part_base(part) + r] = lse_row;
+        else if (row_valid && lse_out)
+          lse_out[orow] = lse_row;
+      }
+      if (split) {
+        __threadfence();  // this part's rows are visible before it is counted
+        asm volatile("bar.sync 3, %0;" ::"r"(2 * kRows) : "memory");
+        if (tid == 0) *last_flag = atomicAdd(counters + item, 1) == live_parts - 1;
+        asm volatile("bar.sync 3, %0;" ::"r"(2 * kRows) : "memory");
+        write_out = *last_flag;
+        if (write_out && o_ready) {
+          __threadfence();  // the other parts' rows, counted before this one
+          float lq[kMaxKvParts], wq[kMaxKvParts];
+          float M = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kMaxKvParts; ++q) {
+            lq[q] = q < live_parts ? __ldcg(part_lse + part_base(q) + r) : -INFINITY;
+            M = fmaxf(M, lq[q]);
+          }
+          float S = 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxKvParts; ++q) {
+            wq[q] = q < live_parts && lq[q] != -INFINITY ? ex2((lq[q] - M) * kLog2e) : 0.f;
+            S += wq[q];
+          }
+          const float invS = S > 0.f ? 1.f / S : 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxKvParts; ++q) wq[q] *= invS;
+#pragma unroll 1
+          for (int c16 = 0; c16 < 16; ++c16) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < kMaxKvParts; ++q) {
+              if (q < live_parts) {
+                const uint4 v = __ldcg(part_o + (part_base(q) / kRows * 16 + c16) * kRows + r);
+                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&vw[e]));
+                  acc[2 * e] = fmaf(wq[q], f.x, acc[2 * e]);
+                  acc[2 * e + 1] = fmaf(wq[q], f.y, acc[2 * e + 1]);
+                }
+              }
+            }
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half2 hh = __floats2half2_rn(acc[2 * e], acc[2 * e + 1]);
+              pk[e] = *reinterpret_cast<const uint32_t *>(&hh);
+            }
+            put(c16, pk);
+          }
+          if (row_valid && lse_out) lse_out[orow] = S > 0.f ? M + lg2(S) * kLn2 : -INFINITY;
+          if (tid == 0) counters[item] = 0;  // ready for the next call
+        }
+      }
     }
     if (full_tile) {  // every thread of the group reaches this barrier
       fence_proxy_async();
       asm volatile("bar.sync %0, %1;" ::"r"(1 + w), "r"(kRows) : "memory");
-      if (r == 0 && !*abort_flag) {
+      if (r == 0 && write_out && !*abort_flag) {
         const int z = q0 + t_lo + w * kQTok;
         tc::tma_store_3d(&tmap_o, stage, 0, g * kGroup, z);
         tc::tma_store_3d(&tmap_o, stage + kQBytes / 2, 64, g * kGroup, z);
@@ -361,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         const int id = dt + kDequantWarps * 32 * i;  // chunks of 16 E4M3 values
         const int pos = id >> 3, c16 = id & 7;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (j * kKv + pos < L) {
+        if ((kv0 + j) * kKv + pos < L) {
           const uint4 raw = *reinterpret_cast<const uint4 *>(vst + pos * 128 + c16 * 16);
           const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t hv[8];
@@ -395,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
         cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
       }
-      const int live = min(kPagesPerTile, (L - j * kKv + kPage - 1) / kPage);
+      const int live = min(kPagesPerTile, (L - (kv0 + j) * kKv + kPage - 1) / kPage);
       int pid = -1;
       if (lane < live) {
         const int pi = j * kPagesPerTile + lane;
@@ -531,7 +657,9 @@ static int32_t set_smem_attr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return K16V8_ERR_CUDA;
   if (dev < 64 && configured[dev]) return K16V8_OK;
-  if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes)) != cudaSuccess ||
+      cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBytes)) != cudaSuccess)
     return K16V8_ERR_CUDA;
   if (dev < 64) configured[dev] = true;
@@ -544,12 +672,52 @@ static int32_t set_smem_attr() {
 using namespace k16v8;
 using namespace k16v8::prefill;
 
-extern "C" int32_t k16v8_paged_prefill_attention(
+// KV parts per work item: kv_splits if given (clamped to 1..4), else the
+// count (1..4) that best fills whole waves of one CTA per SM when the items
+// make less than two waves (with two or more the tail is at most a third of
+// a wave and items are usually short); ties go to fewer parts.
+static int resolve_parts(int32_t kv_splits, int64_t items, int sms) {
+  if (kv_splits > 0) return std::min<int32_t>(kv_splits, kMaxKvParts);
+  if (items <= 0 || sms <= 0 || items >= 2LL * sms) return 1;
+  int best = 1;
+  double best_fill = 0.0;
+  for (int p = 1; p <= kMaxKvParts; ++p) {
+    const double waves = static_cast<double>(items) * p / sms;
+    const double fill = waves / std::ceil(waves - 1e-9);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = p;
+    }
+  }
+  return best;
+}
+
+struct PrefillWs {
+  int parts;
+  size_t counters_off, lse_off, o_off, total;
+};
+
+static PrefillWs prefill_ws(int32_t kv_splits, int32_t max_qlen, int32_t batch,
+                            int32_t num_kv_heads) {
+  PrefillWs w{1, 0, 0, 0, 0};
+  const int64_t max_pairs = (static_cast<int64_t>(max_qlen) + 2 * kQTok - 1) / (2 * kQTok);
+  const int64_t items = max_pairs * num_kv_heads * batch;
+  w.parts = resolve_parts(kv_splits, items, k16v8_sm_count());
+  if (w.parts == 1) return w;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  w.lse_off = up(static_cast<size_t>(items) * 4);
+  w.o_off = w.lse_off + up(static_cast<size_t>(items) * w.parts * 2 * kRows * 4);
+  w.total = w.o_off + static_cast<size_t>(items) * w.parts * 2 * 16 * kRows * 16;
+  return w;
+}
+
+static int32_t prefill_launch(
     const void *q, const int32_t *qo_indptr, int32_t total_q, int32_t max_qlen,
     const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
     int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, void *out,
-    float *lse, int32_t *dev_error, void *stream) {
+    float *lse, int32_t *dev_error, void *stream, int32_t kv_splits, void *workspace,
+    size_t workspace_bytes) {
   if (num_qo_heads <= 0 || num_kv_heads <= 0) return K16V8_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || num_qo_heads != kGroup * num_kv_heads)
     return K16V8_ERR_UNSUPPORTED_SHAPE;
@@ -611,10 +779,54 @@ extern "C" int32_t k16v8_paged_prefill_attention(
   }
   int32_t st = set_smem_attr();
   if (st != K16V8_OK) return st;
-  const dim3 grid((max_qlen + 2 * kQTok - 1) / (2 * kQTok), num_kv_heads, batch);
-  return k16v8_launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes,
-                          static_cast<cudaStream_t>(stream), mq, mk, mo, v_cache, v_scale, qo_indptr,
-                          block_table, max_pages_per_seq, seq_lens, total_q, num_qo_heads,
-                          num_kv_heads, num_pages, sm_scale, static_cast<__half *>(out), lse,
-                          dev_error);
+  const PrefillWs w = prefill_ws(kv_splits, max_qlen, batch, num_kv_heads);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (w.parts > 1 && (!ws || !k16v8_aligned(ws, 256) || workspace_bytes < w.total))
+    return ws ? K16V8_ERR_WORKSPACE_TOO_SMALL : K16V8_ERR_INVALID_ARG;
+  const int64_t max_pairs = (static_cast<int64_t>(max_qlen) + 2 * kQTok - 1) / (2 * kQTok);
+  if (max_pairs * w.parts >= (1LL << 31)) return K16V8_ERR_INVALID_ARG;
+  const dim3 grid(static_cast<unsigned>(max_pairs * w.parts), num_kv_heads, batch);
+  return k16v8_launch_pdl(
+      w.parts > 1 ? prefill_kernel<true> : prefill_kernel<false>, grid, dim3(kThreads),
+      kSmemBytes, static_cast<cudaStream_t>(stream), mq, mk,
+      mo, v_cache, v_scale, qo_indptr, block_table, max_pages_per_seq, seq_lens, total_q,
+      num_qo_heads, num_kv_heads, num_pages, sm_scale, static_cast<__half *>(out), lse, dev_error,
+      static_cast<int32_t>(w.parts),
+      w.parts > 1 ? reinterpret_cast<uint4 *>(ws + w.o_off) : nullptr,
+      w.parts > 1 ? reinterpret_cast<float *>(ws + w.lse_off) : nullptr,
+      w.parts > 1 ? reinterpret_cast<int32_t *>(ws + w.counters_off) : nullptr);
+}
+
+extern "C" int32_t k16v8_paged_prefill_attention(
+    const void *q, const int32_t *qo_indptr, int32_t total_q, int32_t max_qlen,
+    const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
+    int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, void *out,
+    float *lse, int32_t *dev_error, void *stream) {
+  return prefill_launch(q, qo_indptr, total_q, max_qlen, k_cache, v_cache, v_scale, block_table,
+                        max_pages_per_seq, seq_lens, batch, num_qo_heads, num_kv_heads, head_dim,
+                        num_pages, sm_scale, out, lse, dev_error, stream, 1, nullptr, 0);
+}
+
+extern "C" size_t k16v8_prefill_workspace_size(int32_t max_qlen, int32_t batch,
+                                               int32_t num_qo_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t kv_splits) {
+  if (max_qlen <= 0 || batch <= 0 || num_kv_heads <= 0 || head_dim != kHeadDim ||
+      num_qo_heads != kGroup * num_kv_heads || kv_splits < 0)
+    return 0;
+  return prefill_ws(kv_splits, max_qlen, batch, num_kv_heads).total;
+}
+
+extern "C" int32_t k16v8_paged_prefill_attention_split(
+    const void *q, const int32_t *qo_indptr, int32_t total_q, int32_t max_qlen,
+    const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
+    int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, int32_t kv_splits,
+    void *workspace, size_t workspace_bytes, void *out, float *lse, int32_t *dev_error,
+    void *stream) {
+  if (kv_splits < 0) return K16V8_ERR_INVALID_ARG;
+  return prefill_launch(q, qo_indptr, total_q, max_qlen, k_cache, v_cache, v_scale, block_table,
+                        max_pages_per_seq, seq_lens, batch, num_qo_heads, num_kv_heads, head_dim,
+                        num_pages, sm_scale, out, lse, dev_error, stream, kv_splits, workspace,
+                        workspace_bytes);
 }

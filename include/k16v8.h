@@ -387,6 +387,45 @@ int32_t k16v8_paged_prefill_attention(const void *q, const int32_t *qo_indptr,
                                       float *lse, int32_t *dev_error, void *stream);
 
 /*
+ * paged_prefill_attention_split -- the same causal prefill with the KV range
+ * of each work item (a pair of 32-token query tiles of one sequence and KV
+ * head) cut into up to 4 parts that run as separate CTAs, for calls whose
+ * items would not fill the GPU in whole waves (e.g. one 1,024-token chunk of
+ * one prompt: 16 pairs x 10 KV heads = 160 items on 152 SMs leaves a
+ * near-empty second wave).  Every part writes its rows normalised by its own
+ * softmax sum (fp16) and their LSE to the workspace; the part that finishes
+ * last (an atomic counter per item, no waiting) combines them,
+ * o = sum_p e^(lse_p - lse) o_p with lse = log sum_p e^lse_p, and writes out
+ * and lse.  The fp16 rounding of the parts adds at most one fp16 ulp of each
+ * part's share to the fp16 output.
+ *   kv_splits   0: chosen from max_qlen, batch, num_kv_heads and the SM
+ *               count (1 unless the items make less than two waves, then
+ *               the count of 1..4 that best fills whole waves); 1..4 forced.
+ *               A part holds at least 8 KV tiles (1,024 positions), so items
+ *               with fewer than 16 tiles are not split whatever the count.
+ *   workspace   device, k16v8_prefill_workspace_size(max_qlen, batch,
+ *               num_qo_heads, num_kv_heads, head_dim, kv_splits) bytes
+ *               (0: no split, NULL allowed), 256-B aligned, zero-filled
+ *               before its first use; a call that raises no device error
+ *               leaves it ready for the next call (its counters back at 0).
+ *               Calls that overlap on the GPU must not share one.
+ * Other arguments, outputs and errors as for k16v8_paged_prefill_attention;
+ * K16V8_ERR_WORKSPACE_TOO_SMALL if workspace_bytes is short,
+ * K16V8_ERR_INVALID_ARG for kv_splits < 0 or a NULL / unaligned workspace
+ * that is needed.
+ */
+size_t k16v8_prefill_workspace_size(int32_t max_qlen, int32_t batch, int32_t num_qo_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t kv_splits);
+
+int32_t k16v8_paged_prefill_attention_split(
+    const void *q, const int32_t *qo_indptr, int32_t total_q, int32_t max_qlen,
+    const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
+    int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, int32_t kv_splits,
+    void *workspace, size_t workspace_bytes, void *out, float *lse, int32_t *dev_error,
+    void *stream);
+
+/*
  * paged_decode_attention_static -- the same computation as
  * k16v8_paged_decode_attention, for callers that cannot allocate device
  * memory: a host that runs inside an engine whose memory manager owns every

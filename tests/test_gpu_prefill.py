@@ -21,11 +21,19 @@ def K():
     return k16v8
 
 
-def run_calls(K, p, rows_to_check=None, err=None):
+def run_calls(K, p, rows_to_check=None, err=None, kv_splits=None):
     """Append + prefill for every call of a PrefillInputs; returns
-    {call index: (out, lse)} on the host."""
+    {call index: (out, lse)} on the host.  kv_splits: None for the plain
+    call, else the split call with that count (0 = its own choice) and one
+    zero-filled workspace shared by all calls."""
     kc, vc = gpu_poisoned_caches(p.num_pages, p.num_kv_heads, p.head_dim)
     vs = to_dev(p.v_scale)
+    ws = None
+    if kv_splits is not None:
+        n = max(K.k16v8_prefill_workspace_size(int(c.qlens.max()), len(c.seq_lens),
+                                               p.num_qo_heads, p.num_kv_heads, p.head_dim,
+                                               kv_splits) for c in p.calls)
+        ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev())
     res = []
     for call in p.calls:
         rows = call.rows
@@ -34,9 +42,15 @@ def run_calls(K, p, rows_to_check=None, err=None):
         q = to_dev(p.q[rows])
         out = torch.full(q.shape, float("nan"), dtype=torch.float16, device=dev())
         lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=dev())
-        K.k16v8_paged_prefill_attention(q, to_dev(call.qo_indptr), int(call.qlens.max()), kc, vc,
-                                        vs, to_dev(call.block_table), to_dev(call.seq_lens),
-                                        p.sm_scale, out, lse, err)
+        if kv_splits is None:
+            K.k16v8_paged_prefill_attention(q, to_dev(call.qo_indptr), int(call.qlens.max()), kc,
+                                            vc, vs, to_dev(call.block_table),
+                                            to_dev(call.seq_lens), p.sm_scale, out, lse, err)
+        else:
+            K.k16v8_paged_prefill_attention_split(
+                q, to_dev(call.qo_indptr), int(call.qlens.max()), kc, vc, vs,
+                to_dev(call.block_table), to_dev(call.seq_lens), p.sm_scale, ws, out, lse, err,
+                kv_splits=kv_splits)
         res.append((out.float().cpu().numpy(), lse.cpu().numpy()))
     return res
 
@@ -94,3 +108,52 @@ def test_prefill_bad_page_is_flagged(K):
     err = torch.zeros(1, dtype=torch.int32, device=dev())
     run_calls(K, p, err=err)
     assert K.k16v8_read_device_error(err) & K.DEVERR_PAGE
+
+
+@pytest.mark.parametrize("kv_splits", [2, 3, 4])
+def test_prefill_kv_split_forced(K, kv_splits):
+    """Long prefixes (up to 4,600 positions: up to 36 KV tiles, so up to 4
+    parts of >= 8) and short ones (not split) in the same calls; one
+    workspace across the calls, so the per-item counters must come back to
+    zero after every call."""
+    p = workloads.make_prefill("split", 10, [4600, 2100, 700], chunk=1024, num_qo_heads=8,
+                               num_kv_heads=2)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    res = run_calls(K, p, err=err, kv_splits=kv_splits)
+    assert K.k16v8_read_device_error(err) == 0
+    check_against_oracle(p, res, sample=5)
+
+
+def test_prefill_1x8k_kv_split_auto_sampled(K):
+    """The 8192-token prompt in 8 chunks: 160 items per call on the GPU's SMs,
+    so the split call picks more than one part."""
+    p = workloads.prefill_1x8k()
+    call = p.calls[-1]
+    assert K.k16v8_prefill_workspace_size(int(call.qlens.max()), 1, 40, 10, 128, 0) > 0
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    res = run_calls(K, p, err=err, kv_splits=0)
+    assert K.k16v8_read_device_error(err) == 0
+    check_against_oracle(p, res, sample=41)
+
+
+def test_prefill_kv_split_host_checks(K):
+    p = workloads.make_prefill("hc", 11, [2048], chunk=1024, num_qo_heads=8, num_kv_heads=2)
+    call = p.calls[0]
+    n = K.k16v8_prefill_workspace_size(1024, 1, 8, 2, 128, 2)
+    assert n > 0 and K.k16v8_prefill_workspace_size(1024, 1, 8, 2, 128, 1) == 0
+    assert K.k16v8_prefill_workspace_size(1024, 1, 8, 2, 64, 2) == 0
+    kc, vc = gpu_poisoned_caches(p.num_pages, p.num_kv_heads, p.head_dim)
+    q = to_dev(p.q[call.rows])
+    out = torch.empty(q.shape, dtype=torch.float16, device=dev())
+    small = torch.zeros(n - 256, dtype=torch.uint8, device=dev())
+    args = (q, to_dev(call.qo_indptr), 1024, kc, vc, to_dev(p.v_scale), to_dev(call.block_table),
+            to_dev(call.seq_lens), p.sm_scale)
+    with pytest.raises(K.K16V8Error) as e:
+        K.k16v8_paged_prefill_attention_split(*args, small, out, kv_splits=2)
+    assert e.value.status == K.K16V8_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(K.K16V8Error) as e:
+        K.k16v8_paged_prefill_attention_split(*args, None, out, kv_splits=2)
+    assert e.value.status == K.K16V8_ERR_INVALID_ARG
+    with pytest.raises(K.K16V8Error) as e:
+        K.k16v8_paged_prefill_attention_split(*args, small, out, kv_splits=-1)
+    assert e.value.status == K.K16V8_ERR_INVALID_ARG
