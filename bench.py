@@ -593,8 +593,10 @@ class PrefillBench:
                 out=torch.empty(q.shape, dtype=torch.float16, device=device),
                 lse=torch.empty(q.shape[:2], dtype=torch.float32, device=device)))
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        for c, pc in zip(self.calls, p.calls):
+            c["max_len"] = int(pc.seq_lens.max())  # the scheduler knows its lengths
         n = max(K.k16v8_prefill_workspace_size(c["max_qlen"], len(pc.seq_lens), p.num_qo_heads,
-                                               p.num_kv_heads, p.head_dim, 0)
+                                               p.num_kv_heads, p.head_dim, 0, c["max_len"])
                 for c, pc in zip(self.calls, p.calls))
         self.ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
         self.ws_bytes = n
@@ -606,7 +608,7 @@ class PrefillBench:
         if self.split:
             self.K.k16v8_paged_prefill_attention_split(
                 c["q"], c["indptr"], c["max_qlen"], self.kc, self.vc, self.vs, c["bt"], c["lens"],
-                self.p.sm_scale, self.ws, c["out"], c["lse"], self.err)
+                self.p.sm_scale, self.ws, c["out"], c["lse"], self.err, max_seq_len=c["max_len"])
         else:
             self.K.k16v8_paged_prefill_attention(c["q"], c["indptr"], c["max_qlen"], self.kc,
                                                  self.vc, self.vs, c["bt"], c["lens"],

@@ -675,13 +675,21 @@ using namespace k16v8::prefill;
 // KV parts per work item: kv_splits if given (clamped to 1..4), else the
 // count (1..4) that best fills whole waves of one CTA per SM when the items
 // make less than two waves (with two or more the tail is at most a third of
-// a wave and items are usually short); ties go to fewer parts.
-static int resolve_parts(int32_t kv_splits, int64_t items, int sms) {
+// a wave and items are usually short); ties go to fewer parts.  A known
+// bound on the cached length caps the count at what the longest pair can
+// use (the kernel gives a pair at most one part per 8 KV tiles), so a call
+// over short prefixes launches no CTAs that would find nothing to do.
+static int resolve_parts(int32_t kv_splits, int64_t items, int sms, int32_t max_seq_len) {
   if (kv_splits > 0) return std::min<int32_t>(kv_splits, kMaxKvParts);
   if (items <= 0 || sms <= 0 || items >= 2LL * sms) return 1;
+  int cap = kMaxKvParts;
+  if (max_seq_len > 0)
+    cap = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(kMaxKvParts,
+                             ((static_cast<int64_t>(max_seq_len) + kKv - 1) / kKv) / kMinPartTiles)));
   int best = 1;
   double best_fill = 0.0;
-  for (int p = 1; p <= kMaxKvParts; ++p) {
+  for (int p = 1; p <= cap; ++p) {
     const double waves = static_cast<double>(items) * p / sms;
     const double fill = waves / std::ceil(waves - 1e-9);
     if (fill > best_fill + 1e-9) {
@@ -698,11 +706,11 @@ struct PrefillWs {
 };
 
 static PrefillWs prefill_ws(int32_t kv_splits, int32_t max_qlen, int32_t batch,
-                            int32_t num_kv_heads) {
+                            int32_t num_kv_heads, int32_t max_seq_len) {
   PrefillWs w{1, 0, 0, 0, 0};
   const int64_t max_pairs = (static_cast<int64_t>(max_qlen) + 2 * kQTok - 1) / (2 * kQTok);
   const int64_t items = max_pairs * num_kv_heads * batch;
-  w.parts = resolve_parts(kv_splits, items, k16v8_sm_count());
+  w.parts = resolve_parts(kv_splits, items, k16v8_sm_count(), max_seq_len);
   if (w.parts == 1) return w;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   w.lse_off = up(static_cast<size_t>(items) * 4);
@@ -716,8 +724,8 @@ static int32_t prefill_launch(
     const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
     int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, void *out,
-    float *lse, int32_t *dev_error, void *stream, int32_t kv_splits, void *workspace,
-    size_t workspace_bytes) {
+    float *lse, int32_t *dev_error, void *stream, int32_t kv_splits, int32_t max_seq_len,
+    void *workspace, size_t workspace_bytes) {
   if (num_qo_heads <= 0 || num_kv_heads <= 0) return K16V8_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || num_qo_heads != kGroup * num_kv_heads)
     return K16V8_ERR_UNSUPPORTED_SHAPE;
@@ -779,7 +787,7 @@ static int32_t prefill_launch(
   }
   int32_t st = set_smem_attr();
   if (st != K16V8_OK) return st;
-  const PrefillWs w = prefill_ws(kv_splits, max_qlen, batch, num_kv_heads);
+  const PrefillWs w = prefill_ws(kv_splits, max_qlen, batch, num_kv_heads, max_seq_len);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   if (w.parts > 1 && (!ws || !k16v8_aligned(ws, 256) || workspace_bytes < w.total))
     return ws ? K16V8_ERR_WORKSPACE_TOO_SMALL : K16V8_ERR_INVALID_ARG;
@@ -805,16 +813,17 @@ extern "C" int32_t k16v8_paged_prefill_attention(
     float *lse, int32_t *dev_error, void *stream) {
   return prefill_launch(q, qo_indptr, total_q, max_qlen, k_cache, v_cache, v_scale, block_table,
                         max_pages_per_seq, seq_lens, batch, num_qo_heads, num_kv_heads, head_dim,
-                        num_pages, sm_scale, out, lse, dev_error, stream, 1, nullptr, 0);
+                        num_pages, sm_scale, out, lse, dev_error, stream, 1, 0, nullptr, 0);
 }
 
 extern "C" size_t k16v8_prefill_workspace_size(int32_t max_qlen, int32_t batch,
                                                int32_t num_qo_heads, int32_t num_kv_heads,
-                                               int32_t head_dim, int32_t kv_splits) {
+                                               int32_t head_dim, int32_t kv_splits,
+                                               int32_t max_seq_len) {
   if (max_qlen <= 0 || batch <= 0 || num_kv_heads <= 0 || head_dim != kHeadDim ||
-      num_qo_heads != kGroup * num_kv_heads || kv_splits < 0)
+      num_qo_heads != kGroup * num_kv_heads || kv_splits < 0 || max_seq_len < 0)
     return 0;
-  return prefill_ws(kv_splits, max_qlen, batch, num_kv_heads).total;
+  return prefill_ws(kv_splits, max_qlen, batch, num_kv_heads, max_seq_len).total;
 }
 
 extern "C" int32_t k16v8_paged_prefill_attention_split(
@@ -822,11 +831,11 @@ extern "C" int32_t k16v8_paged_prefill_attention_split(
     const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
     int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, int32_t kv_splits,
-    void *workspace, size_t workspace_bytes, void *out, float *lse, int32_t *dev_error,
-    void *stream) {
-  if (kv_splits < 0) return K16V8_ERR_INVALID_ARG;
+    int32_t max_seq_len, void *workspace, size_t workspace_bytes, void *out, float *lse,
+    int32_t *dev_error, void *stream) {
+  if (kv_splits < 0 || max_seq_len < 0) return K16V8_ERR_INVALID_ARG;
   return prefill_launch(q, qo_indptr, total_q, max_qlen, k_cache, v_cache, v_scale, block_table,
                         max_pages_per_seq, seq_lens, batch, num_qo_heads, num_kv_heads, head_dim,
-                        num_pages, sm_scale, out, lse, dev_error, stream, kv_splits, workspace,
-                        workspace_bytes);
+                        num_pages, sm_scale, out, lse, dev_error, stream, kv_splits, max_seq_len,
+                        workspace, workspace_bytes);
 }

@@ -66,10 +66,10 @@ SIGNATURES = {
     "k16v8_paged_prefill_attention": (_i32, [_P, _P, _i32, _i32, _P, _P, _P, _P, _i32, _P,
                                              _i32, _i32, _i32, _i32, _i32, _f32, _P, _P, _P,
                                              _P]),
-    "k16v8_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "k16v8_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "k16v8_paged_prefill_attention_split": (_i32, [_P, _P, _i32, _i32, _P, _P, _P, _P, _i32,
                                                    _P, _i32, _i32, _i32, _i32, _i32, _f32,
-                                                   _i32, _P, _sz, _P, _P, _P, _P]),
+                                                   _i32, _i32, _P, _sz, _P, _P, _P, _P]),
     "k16v8_decode_balanced_workspace_size": (_sz, [_i32, _i32, _i32]),
     "k16v8_paged_decode_attention_balanced": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32,
                                                      _i32, _i32, _i32, _f32, _P, _sz, _P, _P,
@@ -296,16 +296,18 @@ def k16v8_paged_prefill_attention(q, qo_indptr, max_qlen, k_cache, v_cache, v_sc
 
 
 def k16v8_prefill_workspace_size(max_qlen, batch, num_qo_heads, num_kv_heads, head_dim,
-                                 kv_splits=0) -> int:
+                                 kv_splits=0, max_seq_len=0) -> int:
     """Bytes of workspace k16v8_paged_prefill_attention_split needs (0: the
     call will not split, no workspace needed)."""
     return int(load_library().k16v8_prefill_workspace_size(max_qlen, batch, num_qo_heads,
-                                                            num_kv_heads, head_dim, kv_splits))
+                                                            num_kv_heads, head_dim, kv_splits,
+                                                            max_seq_len))
 
 
 def k16v8_paged_prefill_attention_split(q, qo_indptr, max_qlen, k_cache, v_cache, v_scale,
                                         block_table, seq_lens, sm_scale, workspace, out,
-                                        lse=None, dev_error=None, stream=None, kv_splits=0):
+                                        lse=None, dev_error=None, stream=None, kv_splits=0,
+                                        max_seq_len=0):
     """Prefill attention with the KV range of each query-tile pair cut into
     up to 4 parts (merged in the kernel) when the call has too few pairs to
     fill the GPU; `workspace` zero-filled before its first use."""
@@ -315,7 +317,8 @@ def k16v8_paged_prefill_attention_split(q, qo_indptr, max_qlen, k_cache, v_cache
         _ptr(q), _ptr(qo_indptr), total_q, int(max_qlen), _ptr(k_cache), _ptr(v_cache),
         _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
         seq_lens.shape[0], hq, k_cache.shape[1], d, k_cache.shape[0], float(sm_scale),
-        int(kv_splits), _ptr(workspace), nbytes, _ptr(out), _ptr(lse), _ptr(dev_error),
+        int(kv_splits), int(max_seq_len), _ptr(workspace), nbytes, _ptr(out), _ptr(lse),
+        _ptr(dev_error),
         _stream(stream))
     _check("k16v8_paged_prefill_attention_split", st)
 

@@ -403,27 +403,34 @@ int32_t k16v8_paged_prefill_attention(const void *q, const int32_t *qo_indptr,
  *               the count of 1..4 that best fills whole waves); 1..4 forced.
  *               A part holds at least 8 KV tiles (1,024 positions), so items
  *               with fewer than 16 tiles are not split whatever the count.
+ *   max_seq_len an upper bound on this call's seq_lens, or 0 if unknown: with
+ *               kv_splits = 0 it caps the parts at what the longest pair can
+ *               use (one per 8 KV tiles), so calls over short prefixes
+ *               launch no CTAs that would find nothing to do.  Only a hint:
+ *               longer sequences are still computed correctly.
  *   workspace   device, k16v8_prefill_workspace_size(max_qlen, batch,
- *               num_qo_heads, num_kv_heads, head_dim, kv_splits) bytes
+ *               num_qo_heads, num_kv_heads, head_dim, kv_splits,
+ *               max_seq_len) bytes
  *               (0: no split, NULL allowed), 256-B aligned, zero-filled
  *               before its first use; a call that raises no device error
  *               leaves it ready for the next call (its counters back at 0).
  *               Calls that overlap on the GPU must not share one.
  * Other arguments, outputs and errors as for k16v8_paged_prefill_attention;
  * K16V8_ERR_WORKSPACE_TOO_SMALL if workspace_bytes is short,
- * K16V8_ERR_INVALID_ARG for kv_splits < 0 or a NULL / unaligned workspace
- * that is needed.
+ * K16V8_ERR_INVALID_ARG for kv_splits < 0, max_seq_len < 0 or a NULL /
+ * unaligned workspace that is needed.
  */
 size_t k16v8_prefill_workspace_size(int32_t max_qlen, int32_t batch, int32_t num_qo_heads,
-                                    int32_t num_kv_heads, int32_t head_dim, int32_t kv_splits);
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t kv_splits,
+                                    int32_t max_seq_len);
 
 int32_t k16v8_paged_prefill_attention_split(
     const void *q, const int32_t *qo_indptr, int32_t total_q, int32_t max_qlen,
     const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
     int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, int32_t kv_splits,
-    void *workspace, size_t workspace_bytes, void *out, float *lse, int32_t *dev_error,
-    void *stream);
+    int32_t max_seq_len, void *workspace, size_t workspace_bytes, void *out, float *lse,
+    int32_t *dev_error, void *stream);
 
 /*
  * paged_decode_attention_static -- the same computation as

@@ -21,7 +21,7 @@ def K():
     return k16v8
 
 
-def run_calls(K, p, rows_to_check=None, err=None, kv_splits=None):
+def run_calls(K, p, rows_to_check=None, err=None, kv_splits=None, max_seq_len_hint=False):
     """Append + prefill for every call of a PrefillInputs; returns
     {call index: (out, lse)} on the host.  kv_splits: None for the plain
     call, else the split call with that count (0 = its own choice) and one
@@ -50,7 +50,7 @@ def run_calls(K, p, rows_to_check=None, err=None, kv_splits=None):
             K.k16v8_paged_prefill_attention_split(
                 q, to_dev(call.qo_indptr), int(call.qlens.max()), kc, vc, vs,
                 to_dev(call.block_table), to_dev(call.seq_lens), p.sm_scale, ws, out, lse, err,
-                kv_splits=kv_splits)
+                kv_splits=kv_splits, max_seq_len=max_seq_len_hint and int(call.seq_lens.max()))
         res.append((out.float().cpu().numpy(), lse.cpu().numpy()))
     return res
 
@@ -126,14 +126,21 @@ def test_prefill_kv_split_forced(K, kv_splits):
 
 def test_prefill_1x8k_kv_split_auto_sampled(K):
     """The 8192-token prompt in 8 chunks: 160 items per call on the GPU's SMs,
-    so the split call picks more than one part."""
+    so the split call picks more than one part (no length hint here); with
+    a length bound the first chunk (prefix <= 1024: 8 KV tiles) is not
+    split."""
     p = workloads.prefill_1x8k()
     call = p.calls[-1]
     assert K.k16v8_prefill_workspace_size(int(call.qlens.max()), 1, 40, 10, 128, 0) > 0
+    assert K.k16v8_prefill_workspace_size(1024, 1, 40, 10, 128, 0, 1024) == 0
+    assert K.k16v8_prefill_workspace_size(1024, 1, 40, 10, 128, 0, 8192) > 0
     err = torch.zeros(1, dtype=torch.int32, device=dev())
     res = run_calls(K, p, err=err, kv_splits=0)
     assert K.k16v8_read_device_error(err) == 0
     check_against_oracle(p, res, sample=41)
+    res2 = run_calls(K, p, err=err, kv_splits=0, max_seq_len_hint=True)
+    assert K.k16v8_read_device_error(err) == 0
+    check_against_oracle(p, res2, sample=41)
 
 
 def test_prefill_kv_split_host_checks(K):
@@ -156,4 +163,7 @@ def test_prefill_kv_split_host_checks(K):
     assert e.value.status == K.K16V8_ERR_INVALID_ARG
     with pytest.raises(K.K16V8Error) as e:
         K.k16v8_paged_prefill_attention_split(*args, small, out, kv_splits=-1)
+    assert e.value.status == K.K16V8_ERR_INVALID_ARG
+    with pytest.raises(K.K16V8Error) as e:
+        K.k16v8_paged_prefill_attention_split(*args, small, out, max_seq_len=-1)
     assert e.value.status == K.K16V8_ERR_INVALID_ARG
