@@ -357,15 +357,16 @@ class DecodeBench:
             outs.append(t0.elapsed_time(t1) / steps)
         return np.array([outs])
 
-    def run_e2e(self, steps, warmup):
+    def run_e2e(self, steps, warmup, nbuf=3):
         """Same steps through host buffers.  Every step copies its inputs (q,
         the new K/V rows, lengths, block table, slots) from one pinned host
         buffer to the device in one copy, runs the launches, and reads out +
         lse back into a pinned host buffer in one copy, all inside the timed
         region (host wall clock).  The copies are pipelined as a serving loop
-        would: step i+1's inputs go up (copy stream) and step i-1's results
-        come down (a second copy stream) while step i computes, with two
-        device buffers each way; every step still moves all of its bytes.
+        would: later steps' inputs go up (copy stream) and earlier steps'
+        results come down (a second copy stream) while step i computes, with
+        `nbuf` device buffers each way; every step still moves all of its
+        bytes.
         The steps are captured back to back in one CUDA graph."""
         torch, K, w = self.torch, self.K, self.w
         align = lambda n: (n + 255) // 256 * 256
@@ -386,9 +387,9 @@ class DecodeBench:
             h_in.append(buf)
         o_bytes = self.out.numel() * 2
         out_total = align(o_bytes) + self.lse.numel() * 4
-        d_in = [torch.empty(total, dtype=torch.uint8, device=self.dev) for _ in range(2)]
-        d_out = [torch.empty(out_total, dtype=torch.uint8, device=self.dev) for _ in range(2)]
-        h_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        d_in = [torch.empty(total, dtype=torch.uint8, device=self.dev) for _ in range(nbuf)]
+        d_out = [torch.empty(out_total, dtype=torch.uint8, device=self.dev) for _ in range(nbuf)]
+        h_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(nbuf)]
 
         def views(k):
             v = lambda name, t: d_in[k][offs[name]:offs[name] + t.numel() * t.element_size()] \
@@ -398,35 +399,39 @@ class DecodeBench:
             d["lse"] = d_out[k][align(o_bytes):].view(torch.float32).view(self.lse.shape)
             return d
 
-        dv = [views(0), views(1)]
+        dv = [views(k) for k in range(nbuf)]
         h2d = sum(t.numel() * t.element_size() for _, t in parts)
         d2h = o_bytes + self.lse.numel() * 4
 
-        def compute(d):
+        def split_launches(d):  # the step's launches up to the attention split
             if self.mode == "balanced_fused":
-                K.k16v8_paged_decode_append_attention_balanced(
+                K.k16v8_paged_decode_append_balanced_split(
                     d["q"], d["k_new"], d["v_new"], self.kc, self.vc, self.v_scale, d["bt"],
                     d["seq_lens"], w.sm_scale, self.ws, d["out"], d["lse"], self.err,
                     flags=K.DECODE_METADATA_READY)
-                return
-            if self.mode == "fused":
-                K.k16v8_paged_decode_append_attention(
+            elif self.mode == "fused":
+                K.k16v8_paged_decode_append_split(
                     d["q"], d["k_new"], d["v_new"], self.kc, self.vc, self.v_scale, d["bt"],
-                    d["seq_lens"], self.max_len, w.sm_scale, self.chunk, self.ws, d["out"],
-                    d["lse"], self.err)
-                return
-            K.k16v8_kv_append(d["k_new"], d["v_new"], d["slots"], self.v_scale, self.kc,
-                              self.vc, self.err)
-            if self.mode == "balanced":
-                K.k16v8_paged_decode_attention_balanced(d["q"], self.kc, self.vc, self.v_scale,
-                                                        d["bt"], d["seq_lens"], w.sm_scale,
-                                                        self.ws, d["out"], d["lse"], self.err,
-                                                        flags=K.DECODE_METADATA_READY)
+                    d["seq_lens"], self.max_len, w.sm_scale, self.chunk, self.ws, self.err)
             else:
-                K.k16v8_paged_decode_attention(d["q"], self.kc, self.vc, self.v_scale, d["bt"],
+                K.k16v8_kv_append(d["k_new"], d["v_new"], d["slots"], self.v_scale, self.kc,
+                                  self.vc, self.err)
+                if self.mode == "balanced":
+                    K.k16v8_paged_decode_balanced_split(
+                        d["q"], self.kc, self.vc, self.v_scale, d["bt"], d["seq_lens"],
+                        w.sm_scale, self.ws, d["out"], d["lse"], self.err,
+                        flags=K.DECODE_METADATA_READY)
+                else:
+                    K.k16v8_paged_decode_split(d["q"], self.kc, self.vc, self.v_scale, d["bt"],
                                                d["seq_lens"], self.max_len, w.sm_scale,
-                                               self.chunk, self.ws, d["out"], d["lse"],
-                                               self.err)
+                                               self.chunk, self.ws, self.err)
+
+        def merge_launch(d):
+            if self.balanced:
+                K.k16v8_merge_balanced(self.ws, w.num_kv_heads, d["out"], d["lse"])
+            else:
+                K.k16v8_merge_states(self.po, self.pl, d["seq_lens"], self.chunk, d["out"],
+                                     d["lse"])
 
         up = torch.cuda.Stream(self.dev)
         down = torch.cuda.Stream(self.dev)
@@ -438,23 +443,32 @@ class DecodeBench:
             in_ready, done, read = [None] * n, [None] * n, [None] * n
             up.wait_stream(main)
             down.wait_stream(main)
-            with torch.cuda.stream(up):
-                d_in[0].copy_(h_in[first % self.R], non_blocking=True)
-                in_ready[0] = ev()
-                in_ready[0].record(up)
+
+            def upload(i):  # step i's inputs into buffer i % nbuf
+                with torch.cuda.stream(up):
+                    if i >= nbuf:
+                        up.wait_event(done[i - nbuf])  # that buffer's last reader is done
+                    d_in[i % nbuf].copy_(h_in[(first + i) % self.R], non_blocking=True)
+                    in_ready[i] = ev()
+                    in_ready[i].record(up)
+
+            for i in range(min(nbuf - 1, n)):
+                upload(i)
+            # A step's waits (its inputs uploaded, its output buffer read back)
+            # go in before the previous step's merge, so that the launches of
+            # consecutive kernels stay adjacent and keep their programmatic
+            # overlap; the order still holds through that merge.
+            main.wait_event(in_ready[0])
             for i in range(n):
-                k = i % 2
-                if i + 1 < n:  # next step's inputs into the other buffer
-                    with torch.cuda.stream(up):
-                        if i >= 1:
-                            up.wait_event(done[i - 1])  # step i-1 has read that buffer
-                        d_in[1 - k].copy_(h_in[(first + i + 1) % self.R], non_blocking=True)
-                        in_ready[i + 1] = ev()
-                        in_ready[i + 1].record(up)
-                main.wait_event(in_ready[i])
-                if i >= 2:
-                    main.wait_event(read[i - 2])  # its output buffer has been read back
-                compute(dv[k])
+                k = i % nbuf
+                if i + nbuf - 1 < n:
+                    upload(i + nbuf - 1)
+                split_launches(dv[k])
+                if i + 1 < n:
+                    main.wait_event(in_ready[i + 1])
+                    if i + 1 >= nbuf:
+                        main.wait_event(read[i + 1 - nbuf])
+                merge_launch(dv[k])
                 done[i] = ev()
                 done[i].record(main)
                 with torch.cuda.stream(down):
@@ -479,10 +493,10 @@ class DecodeBench:
         torch.cuda.synchronize(self.dev)
         dt = (time.perf_counter() - t0) * 1e3 / steps
         barrier()
-        last = dv[(steps - 1) % 2]
+        last = dv[(steps - 1) % nbuf]
         if not torch.equal(last["out"], self.out):
             raise RuntimeError("end-to-end step disagrees with the device-resident step")
-        host = h_out[(steps - 1) % 2][:o_bytes].view(torch.float16).view(self.out.shape)
+        host = h_out[(steps - 1) % nbuf][:o_bytes].view(torch.float16).view(self.out.shape)
         if not torch.equal(host, self.out.cpu()):
             raise RuntimeError("end-to-end result read back to the host disagrees")
         return dt, h2d, d2h
