@@ -1,12 +1,15 @@
 #!/usr/bin/env python3
 """K16/V8 paged decode benchmark (one JSON line on stdout).
 
-A step is one decode layer-step of the whole hot path: kv_append of each
-sequence's new token (FP16 K + E4M3 V), split-KV paged decode attention, and
-the LSE merge, on the Phi-4-shaped workload (40 query / 10 KV heads, d 128,
-16-token pages).  Default workload: decode 1K/batch 32; `--workload 8k`
-selects 8K/batch 16.  The KV pool is replicated so that consecutive steps
-read different copies (the rotation spans >= 4x the L2 size), which keeps the
+A step is one decode layer-step of the whole hot path: the append of each
+sequence's new token (FP16 K + E4M3 V), paged decode attention split over
+the KV sequence, and the LSE merge, on the Phi-4-shaped workload (40 query /
+10 KV heads, d 128, 16-token pages).  The headline schedule folds the append
+into the load-balanced split kernel (2 launches per step); the other
+schedules, the FP16-KV control, the 40-layer full pool and prefill run as
+extra lines.  Default workload: decode 1K/batch 32; `--workload 8k` selects
+8K/batch 16.  The KV pool is replicated so that consecutive steps read
+different copies (the rotation spans >= 4x the L2 size), which keeps the
 timed reads coming from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
