@@ -32,6 +32,16 @@
 // Every hand-off is an mbarrier (transaction counts for copies,
 // tcgen05.commit for MMAs, thread arrivals for softmax and dequant); every
 // wait is bounded.
+//
+// KV-split form (prefill_kernel<true>): for calls whose pairs would not fill
+// the SMs in whole waves, each pair's KV tiles are cut into up to 4 parts run
+// by separate CTAs; every part writes its rows normalised by its own softmax
+// sum (fp16) and their LSE to a workspace and counts itself on a per-pair
+// atomic counter, and the part that completes the count combines the parts
+// (weights e^(lse_p - lse)) and writes the output -- no CTA waits on
+// another.  The plain form is a separate instantiation without that code:
+// compiled into one kernel it cost the plain form 10% through its
+// instruction footprint.
 #include <math.h>
 
 #include <algorithm>
