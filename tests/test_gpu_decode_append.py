@@ -152,3 +152,28 @@ def test_fused_append_balanced_host_checks(K):
             to_dev(w.q), kn, None, kc, vc, to_dev(w.v_scale), to_dev(w.block_table),
             to_dev(w.seq_lens), w.sm_scale, ws, out)
     assert e.value.status == K.K16V8_ERR_INVALID_ARG
+
+
+def test_fused_append_balanced_bad_page_is_flagged(K):
+    """A rejected page id on the page that receives the new token: flagged,
+    and that row lands nowhere in the pool (every other byte as the oracle's
+    append of the other sequences' tokens)."""
+    w = workloads.tiny_decode(5)
+    w.v_tok = w.v_tok.astype(np.float16)
+    kc, vc, okc, ovc = cache_without_new_tokens(w, K)
+    B, hq, d = w.q.shape
+    bt = w.block_table.copy()
+    last = (int(w.seq_lens[1]) - 1) // 16
+    bt[1, last] = w.num_pages + 3
+    nr = w.new_rows
+    ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d), dtype=torch.uint8,
+                     device=dev())
+    out = torch.empty((B, hq, d), dtype=torch.float16, device=dev())
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    K.k16v8_paged_decode_append_attention_balanced(
+        to_dev(w.q), to_dev(w.k_tok[nr]), to_dev(w.v_tok[nr]), kc, vc, to_dev(w.v_scale),
+        to_dev(bt), to_dev(w.seq_lens), w.sm_scale, ws, out, None, err)
+    assert K.k16v8_read_device_error(err) & K.DEVERR_PAGE
+    oracle.kv_append(w.k_tok[nr[:1]], w.v_tok[nr[:1]], w.slot_mapping[nr[:1]], w.v_scale, okc, ovc)
+    hk, hv = host_bits(kc, vc)
+    assert np.array_equal(hk, okc.view(np.uint16)) and np.array_equal(hv, ovc)
