@@ -739,7 +739,8 @@ def fullpool_line(device, steps, warmup, hbm_peak, layers=40, schedule="chunked"
     kvb = layers * int(L.sum()) * 10 * 128 * 3
     del pools, step
     torch.cuda.empty_cache()
-    return {"workload": f"full pool: {layers} layers x {P} pages (223,696 slots, 32 GiB), batch "
+    gib = layers * P * 10 * 16 * 128 * 3 / 2 ** 30
+    return {"workload": f"full pool: {layers} layers x {P} pages (223,696 slots, {gib:.1f} GiB), batch "
                         f"{B}, seq_lens {int(L.min())}..{int(L.max())} (sum {int(L.sum())}, "
                         f"{lay.draws} draw(s)), "
                         + {"chunked": "split 512", "fused": "split 512 with the append folded in",
@@ -868,6 +869,8 @@ def main():
                     help="decode schedule of the main line")
     ap.add_argument("--split-chunk", type=int, default=0,
                     help="tokens per split-KV chunk of the main workload (0: its default)")
+    ap.add_argument("--layers", type=int, default=40,
+                    help="layers of the full-pool workload (fewer for profiling captures)")
     args = ap.parse_args()
     rank, world, local_rank = dist_env()
 
@@ -880,9 +883,9 @@ def main():
         from fp8_paged_kv_append_gb300 import k16v8 as K
         torch.cuda.set_device(0)
         K.load_library()
-        print(json.dumps({"fullpool_40_layers": fullpool_line(
+        print(json.dumps({f"fullpool_{args.layers}_layers": fullpool_line(
             torch.device("cuda", 0), args.steps, max(3, args.warmup), load_peaks()[0],
-            schedule=args.decode)}))
+            layers=args.layers, schedule=args.decode)}))
         return
 
     import torch
