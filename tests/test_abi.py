@@ -84,3 +84,28 @@ def test_host_validation_without_gpu(K):
     assert lib.k16v8_paged_decode_split(*args) == 3
     assert lib.k16v8_merge_states(1, 1, 2, 8, 1, 64, 1, 64, 1, None, None) == 2
     assert lib.k16v8_merge_states(1, 1, -1, 8, 1, 128, 1, 64, 1, None, None) == 1
+
+
+def declared_parameter_counts():
+    """Number of parameters of every k16v8_* function the headers declare."""
+    counts = {}
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            txt = re.sub(r"//[^\n]*", "", txt)
+            for m in re.finditer(r"\b(k16v8_\w+)\s*\(([^;{]*?)\)\s*;", txt, flags=re.S):
+                params = m.group(2).strip()
+                counts[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_binding_signatures_match_header_parameter_counts():
+    """Every ctypes signature takes as many arguments as the C declaration, so
+    a parameter added on one side only fails here, on the CPU."""
+    from fp8_paged_kv_append_gb300 import k16v8
+    counts = declared_parameter_counts()
+    assert len(counts) >= 20
+    for name, n in counts.items():
+        assert name in k16v8.SIGNATURES, name
+        assert len(k16v8.SIGNATURES[name][1]) == n, (name, n, len(k16v8.SIGNATURES[name][1]))
