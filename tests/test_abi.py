@@ -109,3 +109,33 @@ def test_binding_signatures_match_header_parameter_counts():
     for name, n in counts.items():
         assert name in k16v8.SIGNATURES, name
         assert len(k16v8.SIGNATURES[name][1]) == n, (name, n, len(k16v8.SIGNATURES[name][1]))
+
+
+def test_host_validation_of_split_prefill_and_fused_balanced_without_gpu(K):
+    """The newer entry points refuse bad arguments before any CUDA call."""
+    lib = K.load_library()
+    # k16v8_paged_prefill_attention_split: kv_splits / max_seq_len < 0, then shapes
+    pre = [1, 1, 64, 64, 1, 1, 1, 1, 8, 1, 1, 40, 10, 128, 100, 0.1, 0, 0, None, 0, 1, None,
+           None, None]
+    pre[16] = -1
+    assert lib.k16v8_paged_prefill_attention_split(*pre) == 1
+    pre[16], pre[17] = 0, -1
+    assert lib.k16v8_paged_prefill_attention_split(*pre) == 1
+    pre[17], pre[13] = 0, 64  # head_dim 64
+    assert lib.k16v8_paged_prefill_attention_split(*pre) == 2
+    pre[13], pre[12] = 128, 40  # 40 query heads over 40 KV heads: GQA group 1
+    assert lib.k16v8_paged_prefill_attention_split(*pre) == 2
+    pre[12] = 10  # valid shape, but the pointers are not 16-byte aligned
+    assert lib.k16v8_paged_prefill_attention_split(*pre) == 1
+    # k16v8_prefill_workspace_size: 0 for what the call would refuse
+    assert lib.k16v8_prefill_workspace_size(1024, 1, 40, 10, 64, 0, 0) == 0
+    assert lib.k16v8_prefill_workspace_size(1024, 1, 40, 10, 128, -1, 0) == 0
+    assert lib.k16v8_prefill_workspace_size(1024, 1, 40, 10, 128, 0, -1) == 0
+    assert lib.k16v8_prefill_workspace_size(0, 1, 40, 10, 128, 0, 0) == 0
+    # k16v8_paged_decode_append_balanced_split: shapes and batch bound
+    dec = [1, 1, 1, 1, 1, 1, 1, 8, 1, 4, 40, 10, 64, 100, 0.1, 1, 1 << 20, 1, None, 0, None,
+           None]
+    assert lib.k16v8_paged_decode_append_balanced_split(*dec) == 2  # head_dim 64
+    dec[12], dec[9] = 128, 8193
+    assert lib.k16v8_paged_decode_append_balanced_split(*dec) == 1  # batch above 8192
+    assert lib.k16v8_decode_balanced_workspace_size(8193, 40, 128) == 0
