@@ -1,16 +1,20 @@
 #!/usr/bin/env python3
 """K16/V8 paged decode benchmark (one JSON line on stdout).
 
-A step is one decode layer-step of the whole hot path: the append of each
-sequence's new token (FP16 K + E4M3 V), paged decode attention split over
-the KV sequence, and the LSE merge, on the Phi-4-shaped workload (40 query /
-10 KV heads, d 128, 16-token pages).  The headline schedule folds the append
-into the load-balanced split kernel (2 launches per step); the other
-schedules, the FP16-KV control, the 40-layer full pool and prefill run as
-extra lines.  Default workload: decode 1K/batch 32; `--workload 8k` selects
-8K/batch 16.  The KV pool is replicated so that consecutive steps read
-different copies (the rotation spans >= 4x the L2 size), which keeps the
-timed reads coming from HBM.
+The headline is a whole decode step through the 40 layers of the full KV
+pool: per layer a pool of 223,696 token slots (FP16 K + E4M3 V, 32 GiB over
+all layers), batch 64 with ragged lengths in [1, 8192], the Phi-4 geometry
+(40 query / 10 KV heads, d 128, 16-token pages).  Per layer the step appends
+each sequence's new token, runs paged decode attention split over the KV
+sequence and merges the partials (the automatic schedule folds the append
+into the split kernel: 2 launches per layer); the 40 layers are one CUDA
+graph.  `value` is KV GB/s (3,840 B per cached token per layer), with
+`us_per_layer_step` beside it; `roofline` is the attention split kernel's;
+`e2e` runs the same step from pinned host buffers; `cpu_baseline` is the
+oracle on a bounded host sample of the same workload.  Extra lines: decode
+1K/batch 32, prefill with its cache write, the FP16-KV control, and decode
+8K/batch 16 (last).  `--workload 1k|8k` puts a one-layer workload on the main
+line instead; `--workload prefill` prints prefill alone.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -130,17 +134,21 @@ class ClockSampler:
 
 
 MODES = ("chunked", "fused", "balanced", "balanced_fused")
-DEFAULT_DECODE = "balanced_fused"  # schedule of the headline line
+DEFAULT_DECODE = "balanced_fused"  # schedule of a one-layer decode line
 SUFFIX = {"chunked": "chunked", "fused": "fused_append", "balanced": "balanced",
           "balanced_fused": "balanced_fused_append"}
 
-KERNEL_SOURCES = {
-    "chunked": ("decode_split_1k_b32.md", ["decode.cu", "decode_page.cuh", "k16v8_device.cuh"]),
-    "balanced": ("decode_balanced_1k_b32.md",
-                 ["decode_balanced.cu", "decode_page.cuh", "k16v8_device.cuh"]),
-    "balanced_fused": ("decode_balanced_append_1k_b32.md",
-                       ["decode_balanced.cu", "decode_page.cuh", "k16v8_device.cuh"]),
-    "fused": ("decode_split_append_1k_b32.md", ["decode.cu", "decode_page.cuh", "k16v8_device.cuh"]),
+_DECODE_SRC = ["decode.cu", "decode_page.cuh", "k16v8_device.cuh"]
+_BALANCED_SRC = ["decode_balanced.cu", "decode_page.cuh", "k16v8_device.cuh"]
+# (workload, schedule) -> committed ncu summary of its attention kernel and
+# the sources that kernel is built from
+KERNEL_PROFILES = {
+    ("1k", "chunked"): ("decode_split_1k_b32.md", _DECODE_SRC),
+    ("1k", "balanced"): ("decode_balanced_1k_b32.md", _BALANCED_SRC),
+    ("1k", "balanced_fused"): ("decode_balanced_append_1k_b32.md", _BALANCED_SRC),
+    ("8k", "chunked"): ("decode_split_8k_b16.md", _DECODE_SRC),
+    ("8k", "balanced_fused"): ("decode_balanced_append_8k_b16.md", _BALANCED_SRC),
+    ("fullpool", "fused"): ("decode_split_append_fullpool_layer.md", _DECODE_SRC),
 }
 
 
@@ -152,11 +160,13 @@ def sources_sha256(names) -> str:
     return h.hexdigest()
 
 
-def traffic_from_profiles(mode: str):
-    """DRAM bytes per launch of the decode attention kernel of `mode` from the
-    committed ncu summary, or None when its sources changed since that
-    capture."""
-    prof, srcs = KERNEL_SOURCES[mode]
+def traffic_from_profiles(workload: str, mode: str):
+    """DRAM bytes per launch of the attention kernel of (workload, mode) from
+    the committed ncu summary, or None when there is none or its sources
+    changed since that capture."""
+    if (workload, mode) not in KERNEL_PROFILES:
+        return None
+    prof, srcs = KERNEL_PROFILES[(workload, mode)]
     path = os.path.join(ROOT, "profiles", prof)
     if not os.path.exists(path):
         return None
@@ -567,7 +577,9 @@ def fp16_control_line(w, device, chunk, steps, warmup, hbm_peak):
             "split_us": round(times[1] * 1e3, 2),
             "kv_bytes_per_step": kvb, "value": round(kvb / (times[0] * 1e-3) / 1e9, 1),
             "unit": "GB/s",
-            "split_frac_of_hbm_peak": round(split_bytes / (times[1] * 1e-3) / 1e9 / hbm_peak, 4)}
+            "split_frac_of_hbm_peak": round(split_bytes / (times[1] * 1e-3) / 1e9 / hbm_peak, 4),
+            "split_frac_of_nominal": round(split_bytes / (times[1] * 1e-3) / 1e9
+                                           / NOMINAL_HBM_GBS, 4)}
 
 
 # ---- chunked prefill on the GPU --------------------------------------------------
@@ -670,20 +682,35 @@ class PrefillBench:
         return step_ms, attn_ms, app_ms
 
 
-def prefill_line(p, device, steps, warmup, tensor_peak):
+def kv_append_bytes(p) -> int:
+    """Algorithmic bytes of writing every prompt token to the cache: per token
+    and KV head the fp16 K and V rows read (2 + 2 B per element), the fp16 K
+    row and the E4M3 V row written (2 + 1 B per element)."""
+    return int(p.q.shape[0]) * p.num_kv_heads * p.head_dim * (2 + 2 + 2 + 1)
+
+
+def prefill_line(p, device, steps, warmup, tensor_peak, hbm_peak):
     """The prefill calls through the KV-split entry point (the library picks
     the parts; 1 when the items fill the GPU), and the plain call beside it
-    when the split one split anything."""
+    when the split one split anything.  The cache write of the prompts
+    (kv_append, HBM-bound) gets its own roofline."""
     pb = PrefillBench(p, device, split=True)
     step_ms, attn_ms, app_ms = pb.run(steps, warmup)
     fl = prefill_flops(p)
+    ab = kv_append_bytes(p)
     line = {"workload": p.name, "calls": len(p.calls), "query_tokens": int(p.q.shape[0]),
             "ms_per_prompt_batch": round(step_ms, 4),
             "prefill_attention_ms": round(attn_ms, 4), "kv_append_ms": round(app_ms, 4),
             "algorithmic_tflop": round(fl / 1e12, 4),
             "prefill_tflops": round(fl / (attn_ms * 1e-3) / 1e12, 1),
             "frac_of_fp16_tensor_peak": round(fl / (attn_ms * 1e-3) / 1e12 / tensor_peak, 4),
-            "kv_split_workspace_bytes": pb.ws_bytes}
+            "kv_split_workspace_bytes": pb.ws_bytes,
+            "kv_append_roofline": {
+                "bound": "hbm", "kernel": "kv_append_kernel", "launches": len(p.calls),
+                "algorithmic_bytes": ab,
+                "achieved": round(ab / (app_ms * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(ab / (app_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                "frac_of_nominal": round(ab / (app_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4)}}
     if pb.ws_bytes:
         del pb
         plain = PrefillBench(p, device, split=False)
@@ -693,65 +720,275 @@ def prefill_line(p, device, steps, warmup, tensor_peak):
     return line
 
 
-# ---- full-pool ragged decode across 40 layers ------------------------------------
+# ---- full-pool ragged decode across 40 layers (the headline workload) ---------------
 
-def fullpool_line(device, steps, warmup, hbm_peak, layers=40, schedule="chunked"):
-    """One decode step through all layers' attention (per layer: append the new
-    token, split-KV attention, merge) over 32 GiB of pools, replayed as one
-    CUDA graph."""
-    import torch
-    from fp8_paged_kv_append_gb300 import workloads
-    from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
-    lay = workloads.fullpool_layout(seed=4)
-    P, B = lay.num_pages, len(lay.seq_lens)
-    pools = [workloads.device_layer_pool(1000 + l, P, device) for l in range(layers)]
-    g = torch.Generator(device=device)
-    g.manual_seed(44)
-    qs = [torch.randn((B, 40, 128), generator=g, device=device, dtype=torch.float16)
-          for _ in range(layers)]
-    kn = [torch.randn((B, 10, 128), generator=g, device=device, dtype=torch.float16)
-          for _ in range(layers)]
-    vn = [torch.randn((B, 10, 128), generator=g, device=device, dtype=torch.float16)
-          for _ in range(layers)]
+FULLPOOL_SEED = 4
+NOMINAL_HBM_GBS = 8000.0  # nominal GB300 HBM3e bandwidth, for the second fraction
+
+SCHEDULE_TEXT = {
+    "auto": "automatic per batch: the load-balanced split when it gives at most 160 "
+            "(sequence, KV head, page) tiles per CTA, else split-KV chunks of 512 tokens; the "
+            "new token's cache append folded into the split kernel either way; LSE merge",
+    "chunked": "split-KV chunks of 512 tokens (separate append), LSE merge",
+    "fused": "split-KV chunks of 512 tokens with the new token's cache append folded in, "
+             "LSE merge",
+    "balanced": "load-balanced split (one full wave of SMs x 4 CTAs over equal tile ranges, "
+                "separate append), LSE merge of cut segments",
+    "balanced_fused": "load-balanced split with the new token's cache append folded in, LSE "
+                      "merge of cut segments",
+}
+
+
+def fullpool_config(lay, layers, schedule):
+    """The full-pool workload's config (host-side facts only, so the
+    reference arm reports the same one)."""
+    P = lay.num_pages
     L = lay.seq_lens.astype(np.int64)
-    slots = lay.block_table[np.arange(B), (L - 1) // 16].astype(np.int64) * 16 + (L - 1) % 16
-    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
-    step = MultiLayerDecode([p[0] for p in pools], [p[1] for p in pools], [p[2] for p in pools],
-                            td(lay.block_table), td(lay.seq_lens), td(slots), int(L.max()), 40,
-                            split_chunk=512, schedule=schedule)
-    chosen = step.schedule
-    outs = [torch.empty((B, 40, 128), dtype=torch.float16, device=device) for _ in range(layers)]
-    lses = [torch.empty((B, 40), dtype=torch.float32, device=device) for _ in range(layers)]
-    step.capture(qs, kn, vn, outs, lses)
-    for _ in range(warmup):
-        step.replay()
-    torch.cuda.synchronize(device)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        step.replay()
-    t1.record()
-    torch.cuda.synchronize(device)
-    if step.check() != 0:
-        raise RuntimeError("device error flag raised during the full-pool benchmark")
-    ms = t0.elapsed_time(t1) / steps
-    kvb = layers * int(L.sum()) * 10 * 128 * 3
-    del pools, step
-    torch.cuda.empty_cache()
     gib = layers * P * 10 * 16 * 128 * 3 / 2 ** 30
-    return {"workload": f"full pool: {layers} layers x {P} pages (223,696 slots, {gib:.1f} GiB), batch "
-                        f"{B}, seq_lens {int(L.min())}..{int(L.max())} (sum {int(L.sum())}, "
-                        f"{lay.draws} draw(s)), "
-                        + {"chunked": "split 512", "fused": "split 512 with the append folded in",
-                           "balanced": "load-balanced split",
-                           "balanced_fused": "load-balanced split with the append folded in"}
-                        [chosen] + (" (chosen by the tiles-per-CTA rule)" if schedule == "auto"
-                                    else "") + ", one CUDA graph per step",
-            "ms_per_step": round(ms, 4), "us_per_layer_step": round(ms * 1e3 / layers, 2),
-            "kv_bytes_per_step": kvb, "value": round(kvb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
-            "gpu_launches_per_step": (2 if chosen in ("fused", "balanced_fused") else 3) * layers}
+    return {"workload": f"full-pool ragged decode step through {layers} layers: per layer a pool "
+                        f"of {P * 16:,} slots ({P:,} pages of 16 tokens; {gib:.1f} GiB of FP16 K + "
+                        f"E4M3 V over all layers), batch {len(L)}, seq_lens uniform in [1, 8192] "
+                        f"redrawn until the batch fits the pool, 40 q / 10 KV heads, head_dim 128",
+            "layers": layers, "batch": int(len(L)),
+            "seq_lens": f"{int(L.min())}..{int(L.max())}",
+            "cached_tokens_per_layer": int(L.sum()),
+            "schedule": SCHEDULE_TEXT[schedule],
+            "l2": "inputs larger than L2: every step streams the distinct pools of all layers "
+                  f"({layers * int(L.sum()) * 3840 / 1e9:.1f} GB of KV) through the 129 MB L2"}
+
+
+class FullPoolBench:
+    """The decode step through every layer of the 32 GiB pool (per layer: the
+    new token's append, split-KV attention, merge), captured as one CUDA
+    graph per step by MultiLayerDecode."""
+
+    def __init__(self, device, layers=40, schedule="auto"):
+        import torch
+        from fp8_paged_kv_append_gb300 import k16v8 as K
+        from fp8_paged_kv_append_gb300 import workloads
+        from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
+        self.torch, self.K, self.dev, self.layers = torch, K, device, layers
+        self.MLD = MultiLayerDecode
+        self.lay = lay = workloads.fullpool_layout(seed=FULLPOOL_SEED)
+        P, B = lay.num_pages, len(lay.seq_lens)
+        self.B = B
+        self.pools = [workloads.device_layer_pool(1000 + l, P, device) for l in range(layers)]
+        g = torch.Generator(device=device)
+        g.manual_seed(44)
+        rnd = lambda shape: torch.randn(shape, generator=g, device=device, dtype=torch.float16)
+        self.qs = [rnd((B, 40, 128)) for _ in range(layers)]
+        self.kn = [rnd((B, 10, 128)) for _ in range(layers)]
+        self.vn = [rnd((B, 10, 128)) for _ in range(layers)]
+        L = lay.seq_lens.astype(np.int64)
+        self.L = L
+        self.slots = (lay.block_table[np.arange(B), (L - 1) // 16].astype(np.int64) * 16
+                      + (L - 1) % 16)
+        td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.step = self.make_step(td(lay.block_table), td(lay.seq_lens), td(self.slots),
+                                   schedule)
+        self.schedule = self.step.schedule
+        self.outs = [torch.empty((B, 40, 128), dtype=torch.float16, device=device)
+                     for _ in range(layers)]
+        self.lses = [torch.empty((B, 40), dtype=torch.float32, device=device)
+                     for _ in range(layers)]
+        self.step.capture(self.qs, self.kn, self.vn, self.outs, self.lses)
+        torch.cuda.synchronize(device)
+
+    def make_step(self, bt, lens, slots, schedule):
+        return self.MLD([p[0] for p in self.pools], [p[1] for p in self.pools],
+                        [p[2] for p in self.pools], bt, lens, slots, int(self.L.max()), 40,
+                        split_chunk=512, schedule=schedule)
+
+    @property
+    def kv_bytes_per_layer(self) -> int:
+        return int(self.L.sum()) * 10 * 128 * 3
+
+    def run(self, steps, warmup):
+        """ms per whole step: `steps` replays of the step graph between CUDA
+        events on the launching stream, a barrier and a synchronise on both
+        sides."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.step.replay()
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        torch.cuda.synchronize(self.dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            self.step.replay()
+        t1.record()
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        if self.step.check() != 0:
+            raise RuntimeError("device error flag raised during the full-pool benchmark")
+        return t0.elapsed_time(t1) / steps
+
+    def per_kernel(self, reps=2):
+        """Average launch duration (ms) of the attention split and of the
+        merge: one graph per kind holding that launch for every layer (a
+        different pool each), replayed `reps` times between CUDA events on
+        the launching stream."""
+        torch, s = self.torch, self.step
+        res = []
+        for fn in (lambda li: s.split(li, self.qs[li], self.kn[li], self.vn[li], self.outs[li],
+                                      self.lses[li], append=False),
+                   lambda li: s.merge(li, self.outs[li], self.lses[li])):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=torch.cuda.Stream(self.dev),
+                                  capture_error_mode="thread_local"):
+                for li in range(self.layers):
+                    fn(li)
+            g.replay()
+            torch.cuda.synchronize(self.dev)
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(reps):
+                g.replay()
+            t1.record()
+            torch.cuda.synchronize(self.dev)
+            res.append(t0.elapsed_time(t1) / (reps * self.layers))
+        if s.check() != 0:
+            raise RuntimeError("device error flag raised while timing the kernels")
+        return res
+
+    def run_e2e(self, steps, warmup, nbuf=2):
+        """The same step through host buffers, as a serving loop drives it:
+        every step copies all layers' queries and new K/V rows plus the
+        lengths, block table and slots from pinned host memory to the device
+        in one copy, replays the step graph over that buffer, and reads every
+        layer's out + lse back into pinned host memory in one copy.  `nbuf`
+        device buffers each way, so step i+1's inputs go up while step i
+        computes.  Host wall clock over `steps` steps.  Returns (ms per step,
+        H2D bytes per step, D2H bytes per step)."""
+        torch = self.torch
+        align = lambda n: (n + 255) // 256 * 256
+        lay = self.lay
+        meta = [("seq_lens", torch.from_numpy(lay.seq_lens.astype(np.int32))),
+                ("bt", torch.from_numpy(np.ascontiguousarray(lay.block_table.astype(np.int32)))),
+                ("slots", torch.from_numpy(self.slots.astype(np.int64)))]
+        parts = list(meta)
+        for li in range(self.layers):
+            parts += [(f"q{li}", self.qs[li]), (f"k{li}", self.kn[li]), (f"v{li}", self.vn[li])]
+        offs, total = {}, 0
+        for name, t in parts:
+            offs[name] = total
+            total += align(t.numel() * t.element_size())
+        h_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        for name, t in parts:
+            nb = t.numel() * t.element_size()
+            h_in[offs[name]:offs[name] + nb].copy_(t.detach().cpu().contiguous().view(-1)
+                                                  .view(torch.uint8))
+        o_bytes = self.outs[0].numel() * 2
+        l_bytes = self.lses[0].numel() * 4
+        o_stride = align(o_bytes) + align(l_bytes)
+        out_total = self.layers * o_stride
+        d_in = [torch.empty(total, dtype=torch.uint8, device=self.dev) for _ in range(nbuf)]
+        d_out = [torch.empty(out_total, dtype=torch.uint8, device=self.dev) for _ in range(nbuf)]
+        h_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(nbuf)]
+
+        def view(buf, name, like):
+            nb = like.numel() * like.element_size()
+            return buf[offs[name]:offs[name] + nb].view(like.dtype).view(like.shape)
+
+        graphs, outs_k, lses_k = [], [], []
+        for k in range(nbuf):
+            d_in[k].copy_(h_in)
+            sb = self.make_step(view(d_in[k], "bt", meta[1][1]),
+                                view(d_in[k], "seq_lens", meta[0][1]),
+                                view(d_in[k], "slots", meta[2][1]), self.schedule)
+            qs = [view(d_in[k], f"q{li}", self.qs[li]) for li in range(self.layers)]
+            kn = [view(d_in[k], f"k{li}", self.kn[li]) for li in range(self.layers)]
+            vn = [view(d_in[k], f"v{li}", self.vn[li]) for li in range(self.layers)]
+            outs = [d_out[k][li * o_stride:li * o_stride + o_bytes].view(torch.float16)
+                    .view(self.outs[0].shape) for li in range(self.layers)]
+            lses = [d_out[k][li * o_stride + align(o_bytes):li * o_stride + align(o_bytes)
+                             + l_bytes].view(torch.float32).view(self.lses[0].shape)
+                    for li in range(self.layers)]
+            sb.capture(qs, kn, vn, outs, lses)
+            graphs.append(sb)
+            outs_k.append(outs)
+            lses_k.append(lses)
+        torch.cuda.synchronize(self.dev)
+        up = torch.cuda.Stream(self.dev)
+        down = torch.cuda.Stream(self.dev)
+
+        def run(n):
+            main = torch.cuda.current_stream(self.dev)
+            ev = torch.cuda.Event
+            in_ready, done, read = [None] * n, [None] * n, [None] * n
+            up.wait_stream(main)
+            down.wait_stream(main)
+
+            def upload(i):
+                with torch.cuda.stream(up):
+                    if i >= nbuf:
+                        up.wait_event(done[i - nbuf])  # that buffer's last step is done
+                    d_in[i % nbuf].copy_(h_in, non_blocking=True)
+                    in_ready[i] = ev()
+                    in_ready[i].record(up)
+
+            upload(0)
+            for i in range(n):
+                k = i % nbuf
+                if i + 1 < n:
+                    upload(i + 1)
+                main.wait_event(in_ready[i])
+                if i >= nbuf:
+                    main.wait_event(read[i - nbuf])  # its output buffer was read back
+                graphs[k].replay()
+                done[i] = ev()
+                done[i].record(main)
+                with torch.cuda.stream(down):
+                    down.wait_event(done[i])
+                    h_out[k].copy_(d_out[k], non_blocking=True)
+                    read[i] = ev()
+                    read[i].record(down)
+            main.wait_stream(up)
+            main.wait_stream(down)
+
+        run(max(warmup, 2))
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        torch.cuda.synchronize(self.dev)
+        t0 = time.perf_counter()
+        run(steps)
+        torch.cuda.synchronize(self.dev)
+        dt = (time.perf_counter() - t0) * 1e3 / steps
+        barrier()
+        for sb in graphs:
+            if sb.check() != 0:
+                raise RuntimeError("device error flag raised during the end-to-end steps")
+        last = (steps - 1) % nbuf
+        host = h_out[last]
+        for li in range(self.layers):
+            o = host[li * o_stride:li * o_stride + o_bytes].view(torch.float16) \
+                .view(self.outs[0].shape)
+            if not torch.equal(o, self.outs[li].cpu()):
+                raise RuntimeError(f"end-to-end output of layer {li} read back to the host "
+                                   "disagrees with the device-resident step")
+        h2d = sum(t.numel() * t.element_size() for _, t in parts)
+        d2h = self.layers * (o_bytes + l_bytes)
+        del graphs, d_in, d_out
+        return dt, h2d, d2h
+
+
+def fullpool_cpu_sample(nseq=8):
+    """A bounded host-side sample of the full-pool workload for the oracle:
+    `nseq` of its 64 sequences spread over the length range (the shortest,
+    the longest and evenly spaced ranks between), one layer, drawn on the
+    host with the same distributions (K, V fp16 N(0,1), V scales amax/448)."""
+    from fp8_paged_kv_append_gb300 import workloads
+    lay = workloads.fullpool_layout(seed=FULLPOOL_SEED)
+    order = np.argsort(lay.seq_lens, kind="stable")
+    pick = order[np.unique(np.linspace(0, len(order) - 1, nseq).round().astype(int))]
+    lens = lay.seq_lens[pick]
+    w = workloads.make_decode("full-pool sample", 77, lens)
+    desc = (f"one layer, {len(lens)} of the {len(lay.seq_lens)} sequences (lengths "
+            f"{', '.join(str(int(x)) for x in sorted(lens))}; {int(lens.sum())} cached tokens)")
+    return w, desc
 
 
 # ---- CPU baseline: the oracle on the host cores -------------------------------------
@@ -770,15 +1007,19 @@ def oracle_decode_pass(w, okc, ovc, chunk, sample_b, nthreads):
     return int(w.seq_lens[sample_b].astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 3
 
 
-def run_cpu_baseline(w, chunk, budget_s=12.0):
-    """Time the oracle, as it stands, on a bounded sample of the workload."""
+def oracle_cache_for(w):
     import oracle
-    ncores = os.cpu_count() or 1
     okc = np.zeros((w.num_pages, w.num_kv_heads, 16, w.head_dim), np.float16)
     ovc = np.zeros((w.num_pages, w.num_kv_heads, 16, w.head_dim), np.uint8)
     oracle.kv_append(w.k_tok, w.v_tok, w.slot_mapping, w.v_scale, okc, ovc)
-    n = min(w.batch, 4)
-    sample = np.arange(n)
+    return okc, ovc
+
+
+def run_cpu_baseline(w, chunk, sample, desc, budget_s=12.0):
+    """Time the oracle, as it stands, on a bounded sample of the workload:
+    decode passes over sequences `sample` of w until `budget_s` has passed."""
+    ncores = os.cpu_count() or 1
+    okc, ovc = oracle_cache_for(w)
     t0 = time.perf_counter()
     bytes_done = 0
     passes = 0
@@ -791,10 +1032,10 @@ def run_cpu_baseline(w, chunk, budget_s=12.0):
     return {"value": round(bytes_done / el / 1e9, 4), "unit": "GB/s", "cores": ncores,
             "kind": "oracle",
             "sample": f"{passes} oracle decode steps (append + split partials + merge) over "
-                      f"sequences 0..{n - 1} of the workload, {el:.1f} s wall"}
+                      f"{desc}, {el:.1f} s wall"}
 
 
-# ---- main ---------------------------------------------------------------------------
+# ---- decode lines of one layer ------------------------------------------------------
 
 def make_workload(name):
     from fp8_paged_kv_append_gb300 import workloads
@@ -829,22 +1070,39 @@ KERNEL_NAMES = {
 }
 
 
-def decode_line(w, label, chunk, mode, device, steps, hbm_peak):
-    """Secondary decode line: one workload, one schedule."""
+def roofline(algo_bytes, kernel_ms, hbm_peak, peak_kind, kernel, traffic):
+    """The roofline object of an HBM-bound kernel: algorithmic bytes per
+    launch over its average launch duration, against the measured copy
+    bandwidth and, beside it, the nominal HBM3e peak."""
+    achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+            "peak_kind": f"{peak_kind} (copy bandwidth)",
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "nominal_peak": NOMINAL_HBM_GBS, "kernel": kernel,
+            "algorithmic_bytes_per_launch": int(algo_bytes),
+            "kernel_us": round(kernel_ms * 1e3, 2)}
+
+
+def decode_line(w, label, chunk, mode, device, steps, hbm_peak, peak_kind, workload):
+    """One-layer decode line (one workload, one schedule) with the roofline of
+    its attention kernel."""
     import torch
     b = DecodeBench(w, device, split_chunk=chunk, mode=mode)
     ms, seg = b.run(steps, 3)
-    split_name, merge_name, _ = KERNEL_NAMES[mode]
+    split_name, merge_name, kernel = KERNEL_NAMES[mode]
     kvb = kv_bytes(w)
-    s_us = float(np.mean(seg[:, 1])) * 1e3
+    s_ms = float(np.mean(seg[:, 1]))
     sb = kvb + w.batch * w.num_qo_heads * w.head_dim * 2
     out = {"value": round(kvb / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "us_per_layer_step": round(ms * 1e3, 2),
            "kernel_us": {"kv_append": round(float(np.mean(seg[:, 0])) * 1e3, 2),
-                         split_name: round(s_us, 2),
+                         split_name: round(s_ms * 1e3, 2),
                          merge_name: round(float(np.mean(seg[:, 2])) * 1e3, 2)},
-           "split_frac_of_hbm_peak": round(sb / (s_us * 1e-6) / 1e9 / hbm_peak, 4),
+           "roofline": roofline(sb, s_ms, hbm_peak, peak_kind, kernel,
+                                traffic_from_profiles(workload, mode)),
            "step_frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+           "step_frac_of_nominal": round(kvb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
            "config": config_of(w, label, chunk, b.R, mode)}
     if mode in ("fused", "balanced_fused"):
         del out["kernel_us"]["kv_append"]
@@ -854,135 +1112,232 @@ def decode_line(w, label, chunk, mode, device, steps, hbm_peak):
     return out
 
 
-def main():
+# ---- the measured arm ---------------------------------------------------------------
+
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="1k", choices=["1k", "8k", "prefill", "fullpool"])
+    ap.add_argument("--workload", default="fullpool", choices=["fullpool", "1k", "8k", "prefill"])
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the secondary 8K/b16 line inside the JSON")
+                    help="skip the secondary lines (1K/b32, 8K/b16, prefill, FP16-KV control)")
+    ap.add_argument("--all-schedules", action="store_true",
+                    help="also time every decode schedule on 1K/b32, 8K/b16 and the full pool")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--decode", default=DEFAULT_DECODE, choices=list(MODES),
-                    help="decode schedule of the main line")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--decode", default=None, choices=list(MODES) + ["auto"],
+                    help="decode schedule of the main line (default: auto on the full pool, "
+                         "balanced_fused on one layer)")
     ap.add_argument("--split-chunk", type=int, default=0,
-                    help="tokens per split-KV chunk of the main workload (0: its default)")
+                    help="tokens per split-KV chunk of a one-layer workload (0: its default)")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the full-pool workload (fewer for profiling captures)")
-    args = ap.parse_args()
-    rank, world, local_rank = dist_env()
+    args = ap.parse_args(argv)
+    if args.decode is None:
+        args.decode = "auto" if args.workload == "fullpool" else DEFAULT_DECODE
+    if args.decode == "auto" and args.workload != "fullpool":
+        args.decode = DEFAULT_DECODE
+    return args
 
-    if args.impl == "reference":
-        return main_reference(args, rank, world)
-    if args.workload == "prefill":
-        return main_prefill(args)
-    if args.workload == "fullpool":
-        import torch
-        from fp8_paged_kv_append_gb300 import k16v8 as K
-        torch.cuda.set_device(0)
-        K.load_library()
-        print(json.dumps({f"fullpool_{args.layers}_layers": fullpool_line(
-            torch.device("cuda", 0), args.steps, max(3, args.warmup), load_peaks()[0],
-            layers=args.layers, schedule=args.decode)}))
-        return
 
+def measure_fullpool(args, device, rank, world):
+    """The headline: the 40-layer decode step over the 32 GiB pool."""
     import torch
-    import torch.distributed as dist
-    if world > 1:
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    from fp8_paged_kv_append_gb300 import k16v8 as K
-    K.load_library()
+    hbm_peak, _, peak_kind = load_peaks()
+    fb = FullPoolBench(device, layers=args.layers, schedule=args.decode)
+    warm = max(args.warmup, 3)
+    clocks = ClockSampler(device.index or 0).start()
+    ms = fb.run(args.steps, warm)
+    clk = clocks.stop()
+    split_ms, merge_ms = fb.per_kernel()
+    e2e = None
+    if not args.no_e2e:
+        e2e = fb.run_e2e(max(5, args.steps // 2), 3)
+    split_name, merge_name, kernel = KERNEL_NAMES[fb.schedule]
+    algo = fb.kv_bytes_per_layer + fb.B * 40 * 128 * 2
+    units = fb.kv_bytes_per_layer * fb.layers
+    per_layer = fb.step.launches_per_layer()
+    res = {
+        "ms": ms, "units": units, "e2e": e2e,
+        "config": fullpool_config(fb.lay, fb.layers, args.decode),
+        "fields": {
+            "us_per_layer_step": round(ms * 1e3 / fb.layers, 2),
+            "schedule_chosen": fb.schedule,
+            "kernel_us": {split_name: round(split_ms * 1e3, 2),
+                          merge_name: round(merge_ms * 1e3, 2)},
+            "roofline": roofline(algo, split_ms, hbm_peak, peak_kind, kernel,
+                                 traffic_from_profiles("fullpool", fb.schedule)),
+            "step_frac_of_hbm_peak": round(units / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "step_frac_of_nominal": round(units / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+            "gpu_launches": per_layer * fb.layers * args.steps,
+            "clocks": clk}}
+    del fb
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu:
+        w, desc = fullpool_cpu_sample()
+        res["fields"]["cpu_baseline"] = run_cpu_baseline(w, 512, np.arange(w.batch), desc,
+                                                         args.cpu_budget)
+    return res
 
-    # Replicas only: every rank runs the same seeded workload on its own GPU.
+
+def measure_one_layer(args, device, rank, world):
+    """A one-layer decode workload (1K/b32 or 8K/b16) as the main line."""
+    hbm_peak, _, peak_kind = load_peaks()
     w, label, chunk = make_workload(args.workload)
     if args.split_chunk:
         chunk = args.split_chunk
     bench = DecodeBench(w, device, split_chunk=chunk, mode=args.decode)
-    clocks = ClockSampler(local_rank).start()
+    clocks = ClockSampler(device.index or 0).start()
     ms, seg = bench.run(args.steps, max(args.warmup, 3))
     clk = clocks.stop()
-    e2e_ms, h2d, d2h = bench.run_e2e(max(10, args.steps // 2), 3)
+    e2e = None if args.no_e2e else bench.run_e2e(max(10, args.steps // 2), 3)
     kvb = kv_bytes(w)
-    t_ms, units = aggregate(ms, kvb)
-    te_ms, _ = aggregate(e2e_ms, kvb)
-
-    hbm_peak, _, peak_kind = load_peaks()
     B, hq, d = w.q.shape
-    split_us = float(np.mean(seg[:, 1])) * 1e3
-    split_bytes = kvb + B * hq * d * 2
-    achieved = split_bytes / (split_us * 1e-6) / 1e9
-    traffic = traffic_from_profiles(args.decode) if args.workload == "1k" else None
-    split_name, merge_name, kernel_name = KERNEL_NAMES[args.decode]
+    split_ms = float(np.mean(seg[:, 1]))
+    split_name, merge_name, kernel = KERNEL_NAMES[args.decode]
+    fields = {
+        "us_per_layer_step": round(ms * 1e3, 2),
+        "kernel_us": {"kv_append": round(float(np.mean(seg[:, 0])) * 1e3, 2),
+                      split_name: round(split_ms * 1e3, 2),
+                      merge_name: round(float(np.mean(seg[:, 2])) * 1e3, 2)},
+        "roofline": roofline(kvb + B * hq * d * 2, split_ms, hbm_peak, peak_kind, kernel,
+                             traffic_from_profiles(args.workload, args.decode)),
+        "gpu_launches": (2 if args.decode in ("fused", "balanced_fused") else 3) * args.steps,
+        "clocks": clk}
+    if args.decode in ("fused", "balanced_fused"):
+        del fields["kernel_us"]["kv_append"]
+    res = {"ms": ms, "units": kvb, "e2e": e2e, "fields": fields,
+           "config": config_of(w, label, chunk, bench.R, args.decode)}
+    del bench
+    if rank == 0 and world == 1 and not args.no_cpu:
+        n = min(w.batch, 4)
+        fields["cpu_baseline"] = run_cpu_baseline(
+            w, chunk, np.arange(n), f"sequences 0..{n - 1} of the workload", args.cpu_budget)
+    return res
+
+
+def extra_lines(args, device):
+    """Secondary lines: one-layer decode at 1K/b32, prefill with its cache
+    write, the FP16-KV control, and 8K/b16 last (each with the roofline of
+    its dominant kernel)."""
+    import torch
+    from fp8_paged_kv_append_gb300 import workloads
+    hbm_peak, tpeak, peak_kind = load_peaks()
+    n2 = max(10, args.steps // 2)
+    extra = {}
+    w1, l1, c1 = make_workload("1k")
+    w8, l8, c8 = make_workload("8k")
+    if args.workload != "1k":
+        extra["decode_1k_b32"] = decode_line(w1, l1, c1, DEFAULT_DECODE, device, n2, hbm_peak,
+                                             peak_kind, "1k")
+    torch.cuda.empty_cache()
+    extra["prefill"] = {
+        "peak_tflops": tpeak,
+        "peak_kind": f"{peak_kind} dense bf16 (fp16 has the same nominal rate)",
+        "8x1024": prefill_line(workloads.prefill_8x1k(), device, 10, 3, tpeak, hbm_peak),
+        "1x8192_in_8_chunks": prefill_line(workloads.prefill_1x8k(), device, 5, 2, tpeak,
+                                           hbm_peak)}
+    for name, (wf, lf, cf) in (("decode_1k_b32", (w1, l1, c1)), ("decode_8k_b16", (w8, l8, c8))):
+        torch.cuda.empty_cache()
+        ctl = fp16_control_line(wf, device, cf, n2, 3, hbm_peak)
+        ref = decode_line(wf, lf, cf, "chunked", device, n2, hbm_peak, peak_kind, name[7:9])
+        ctl["k16v8_same_split_us_per_layer_step"] = ref["us_per_layer_step"]
+        ctl["k16v8_speedup_over_fp16_kv"] = round(ctl["us_per_layer_step"] /
+                                                  ref["us_per_layer_step"], 3)
+        ctl["compared_with"] = "K16/V8 with the same chunked split (separate append)"
+        extra[f"{name}_fp16_kv_control"] = ctl
+    if args.all_schedules:
+        for m in MODES:
+            for name, (wf, lf, cf) in (("decode_1k_b32", (w1, l1, c1)),
+                                       ("decode_8k_b16", (w8, l8, c8))):
+                extra[f"{name}_{SUFFIX[m]}"] = decode_line(wf, lf, cf, m, device, n2, hbm_peak,
+                                                           peak_kind, name[7:9])
+            torch.cuda.empty_cache()
+            fb = FullPoolBench(device, schedule=m)
+            ms = fb.run(10, 3)
+            extra[f"fullpool_40_layers_{SUFFIX[m]}"] = {
+                "us_per_layer_step": round(ms * 1e3 / 40, 2),
+                "value": round(fb.kv_bytes_per_layer * 40 / (ms * 1e-3) / 1e9, 1),
+                "unit": "GB/s"}
+            del fb
+    if args.workload != "8k":
+        torch.cuda.empty_cache()
+        extra["decode_8k_b16"] = decode_line(w8, l8, c8, DEFAULT_DECODE, device, n2, hbm_peak,
+                                             peak_kind, "8k")
+    return extra
+
+
+def measure_gpu(args, rank, world, local_rank):
+    """Everything this rank measures on its GPU (replicas only: every rank
+    runs the same seeded workload)."""
+    import torch
+    from fp8_paged_kv_append_gb300 import k16v8 as K
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    K.load_library()
+    if args.workload == "fullpool":
+        res = measure_fullpool(args, device, rank, world)
+    else:
+        res = measure_one_layer(args, device, rank, world)
+    if not args.no_extra and rank == 0:
+        res["fields"]["extra"] = extra_lines(args, device)
+    return res
+
+
+def same_config_on_all_ranks(config) -> None:
+    """Replicas must run the same workload: compare every rank's config."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return
+    mine = json.dumps(config, sort_keys=True)
+    allc = [None] * dist.get_world_size()
+    dist.all_gather_object(allc, mine)
+    if any(c != mine for c in allc):
+        raise RuntimeError("ranks ran different workloads")
+
+
+def main(argv=None, backend=None, measure=None):
+    """Parse the flags, set up the ranks (torchrun, replicas only), measure,
+    aggregate (max time, summed units over ranks) and print one JSON line on
+    rank 0.  `backend` / `measure` replace NCCL and the GPU section (tests)."""
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        return main_reference(args, rank, world)
+    if args.workload == "prefill":
+        return main_prefill(args)
+    import torch.distributed as dist
+    if world > 1:
+        if backend is None:
+            import torch
+            torch.cuda.set_device(local_rank)
+            backend = "nccl"
+        dist.init_process_group(backend)
+    res = (measure or measure_gpu)(args, rank, world, local_rank)
+    same_config_on_all_ranks(res["config"])
+    t_ms, units = aggregate(res["ms"], res["units"])
     line = {
         "metric": METRIC, "value": round(units / (t_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
-        "ms_per_step": round(t_ms, 5), "us_per_layer_step": round(t_ms * 1e3, 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "ms_per_step": round(t_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,1) Q/K/V, E4M3 V with per-head amax/448 scales)",
-        "config": config_of(w, label, chunk, bench.R, args.decode),
-        "kernel_us": {"kv_append": round(float(np.mean(seg[:, 0])) * 1e3, 2),
-                      split_name: round(split_us, 2),
-                      merge_name: round(float(np.mean(seg[:, 2])) * 1e3, 2)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": traffic, "peak_kind": f"{peak_kind} (copy bandwidth)",
-                     "kernel": kernel_name,
-                     "algorithmic_bytes_per_launch": split_bytes},
-        "e2e": {"value": round(units / (te_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(te_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": (2 if args.decode in ("fused", "balanced_fused") else 3) * args.steps,
-        "clocks": clk,
-    }
-    if args.decode in ("fused", "balanced_fused"):
-        del line["kernel_us"]["kv_append"]
-    if rank == 0 and world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = run_cpu_baseline(w, chunk, args.cpu_budget)
-    if not args.no_extra and args.workload == "1k":
-        from fp8_paged_kv_append_gb300 import workloads
-        del bench
-        torch.cuda.empty_cache()
-        n2 = max(10, args.steps // 2)
-        w8, label8, chunk8 = make_workload("8k")
-        wls = (("decode_1k_b32", (w, label, chunk)), ("decode_8k_b16", (w8, label8, chunk8)))
-        line["extra"] = {
-            "decode_8k_b16": decode_line(w8, label8, chunk8, args.decode, device, n2, hbm_peak)}
-        for m in MODES:
-            if m != args.decode:
-                for name, (wf, lf, cf) in wls:
-                    line["extra"][f"{name}_{SUFFIX[m]}"] = decode_line(wf, lf, cf, m, device,
-                                                                       n2, hbm_peak)
-        for name, (wf, _, cf) in wls:
-            torch.cuda.empty_cache()
-            ctl = fp16_control_line(wf, device, cf, n2, 3, hbm_peak)
-            ref = line["extra"].get(f"{name}_chunked")
-            k16 = ref["us_per_layer_step"] if ref else (
-                line["us_per_layer_step"] if name == "decode_1k_b32" else
-                line["extra"]["decode_8k_b16"]["us_per_layer_step"])
-            ctl["k16v8_speedup_over_fp16_kv"] = round(ctl["us_per_layer_step"] / k16, 3)
-            ctl["compared_with"] = "K16/V8 with the same chunked split"
-            line["extra"][f"{name}_fp16_kv_control"] = ctl
-        torch.cuda.empty_cache()
-        line["extra"]["fullpool_40_layers"] = fullpool_line(device, 10, 3, hbm_peak,
-                                                            schedule="auto")
-        for m in MODES:
-            line["extra"][f"fullpool_40_layers_{SUFFIX[m]}"] = fullpool_line(
-                device, 10, 3, hbm_peak, schedule=m)
-        _, tpeak, tkind = load_peaks()
-        torch.cuda.empty_cache()
-        line["extra"]["prefill"] = {
-            "peak_tflops": tpeak, "peak_kind": f"{tkind} dense bf16 (fp16 has the same nominal rate)",
-            "8x1024": prefill_line(workloads.prefill_8x1k(), device, 10, 3, tpeak),
-            "1x8192_in_8_chunks": prefill_line(workloads.prefill_1x8k(), device, 5, 2, tpeak)}
+        "config": res["config"]}
+    if res["e2e"] is not None:
+        e_ms, h2d, d2h = res["e2e"]
+        te_ms, _ = aggregate(e_ms, res["units"])
+        line["e2e"] = {"value": round(units / (te_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "ms_per_step": round(te_ms, 4), "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h}
+    line.update(res["fields"])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+    return line
 
 
 def main_prefill(args):
@@ -993,26 +1348,39 @@ def main_prefill(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     K.load_library()
-    _, tpeak, tkind = load_peaks()
+    hbm_peak, tpeak, tkind = load_peaks()
     res = {"8x1024": prefill_line(workloads.prefill_8x1k(), device, args.steps,
-                                  max(3, args.warmup), tpeak)}
+                                  max(3, args.warmup), tpeak, hbm_peak)}
     if not args.no_extra:
         res["1x8192_in_8_chunks"] = prefill_line(workloads.prefill_1x8k(), device, args.steps,
-                                                 max(3, args.warmup), tpeak)
+                                                 max(3, args.warmup), tpeak, hbm_peak)
     print(json.dumps({"prefill": res, "peak_tflops": tpeak, "peak_kind": tkind}), flush=True)
 
 
+def reference_workload(args):
+    """(DecodeInputs, split chunk, sequences per step, sample text, config)
+    of the reference arm, matching the measured arm's config."""
+    if args.workload == "fullpool":
+        from fp8_paged_kv_append_gb300 import workloads
+        w, desc = fullpool_cpu_sample()
+        lay = workloads.fullpool_layout(seed=FULLPOOL_SEED)
+        return w, 512, np.arange(w.batch), desc, fullpool_config(lay, args.layers, args.decode)
+    w, label, chunk = make_workload(args.workload)
+    if args.split_chunk:
+        chunk = args.split_chunk
+    n = min(w.batch, 2)
+    return (w, chunk, np.arange(n), f"sequences 0..{n - 1} of the workload",
+            config_of(w, label, chunk, replicas_for(w), args.decode))
+
+
 def main_reference(args, rank, world):
-    """The reference arm: the oracle, as it stands, on the host cores."""
+    """The reference arm: the oracle, as it stands, on the host cores, on a
+    bounded sample of the same workload (rank 0 only)."""
     if rank != 0:
         return
-    w, label, chunk = make_workload(args.workload)
-    import oracle
-    okc = np.zeros((w.num_pages, w.num_kv_heads, 16, w.head_dim), np.float16)
-    ovc = np.zeros((w.num_pages, w.num_kv_heads, 16, w.head_dim), np.uint8)
-    oracle.kv_append(w.k_tok, w.v_tok, w.slot_mapping, w.v_scale, okc, ovc)
+    w, chunk, sample, desc, config = reference_workload(args)
+    okc, ovc = oracle_cache_for(w)
     ncores = os.cpu_count() or 1
-    sample = np.arange(min(w.batch, 2))
     for _ in range(max(args.warmup, 1)):
         oracle_decode_pass(w, okc, ovc, chunk, sample, ncores)
     t0 = time.perf_counter()
@@ -1025,13 +1393,14 @@ def main_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "impl": "reference", "config": config_of(w, label, chunk, replicas_for(w), args.decode),
+            "impl": "reference", "config": config,
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": ncores, "kind": "oracle",
-                             "sample": f"each step: sequences 0..{len(sample) - 1} of the "
-                                       "workload (append + split partials + merge)"},
+                             "sample": f"each step: one oracle decode step (append + split "
+                                       f"partials + merge) over {desc}"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+    return line
 
 
 if __name__ == "__main__":

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
     const int32_t *__restrict__ seq_lens, int32_t hq, int32_t hkv, int32_t num_pages,
     float sm_scale, int32_t chunk, int32_t max_chunks, float *__restrict__ part_o,
     float *__restrict__ part_lse, const __half *__restrict__ k_new,
-    const __half *__restrict__ v_new, int32_t *dev_error) {
+    const __half *__restrict__ v_new, int32_t *dev_error, int32_t test_skip_page) {
   using Ring = WarpRingT<kVF16 ? 2 * kVPageBytes : kVPageBytes>;
   constexpr uint32_t kVTile = kVF16 ? 2 * kVPageBytes : kVPageBytes;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -91,7 +91,13 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
   const int n_my = warp < n_pages ? (n_pages - warp + kWarps - 1) / kWarps : 0;
   const int64_t head_tile = static_cast<int64_t>(kPage) * kHeadDim;  // elements per (page, head)
   const uint64_t policy = l2_policy_evict_first();
+  // Bounded-wait test hook (test_skip_page >= 0, never in production calls):
+  // warp 0 of the first CTA withholds its copy of page slot test_skip_page
+  // -- no arrival, nothing in flight -- so its wait for that page expires
+  // after kTestPolls polls and the error path below runs.
+  const bool withheld = test_skip_page >= 0 && (c | g | b | warp) == 0;
   auto issue = [&](int k) {
+    if (withheld && k == test_skip_page) return;
     const int s = k % kStages;
     const int pid = page_ids[warp + k * kWarps];
     if (pid < 0) {
@@ -120,7 +126,9 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
   bool ok = true;
   for (; k < n_my; ++k) {
     const int s = k % kStages;
-    ok = __all_sync(kFull, mbar_wait_bounded(&ring.bar[s], (k / kStages) & 1));
+    ok = __all_sync(kFull, mbar_wait_bounded(&ring.bar[s], (k / kStages) & 1,
+                                             withheld && k == test_skip_page ? kTestPolls
+                                                                             : kMaxPolls));
     if (!ok) break;
     const int i = warp + k * kWarps;  // page within the chunk
     const int valid = min(kPage, n_tok - i * kPage);
@@ -141,11 +149,13 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
   }
   if (!ok) {
     // Give up on this chunk: report, then drain the copies still in flight
-    // (bounded) so none lands after the CTA exits.
+    // (bounded) so none lands after the CTA exits.  Pages k .. k+kStages-1
+    // were issued (all but a withheld one); nothing later was.
     if (lane == 0) {
       flag_error(dev_error, K16V8_DEVERR_TIMEOUT);
       for (int kk = k; kk < min(k + kStages, n_my); ++kk)
-        mbar_wait_bounded(&ring.bar[kk % kStages], (kk / kStages) & 1);
+        if (!(withheld && kk == test_skip_page))
+          mbar_wait_bounded(&ring.bar[kk % kStages], (kk / kStages) & 1);
     }
     __syncwarp();
   }
@@ -346,7 +356,7 @@ static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v
                             int32_t num_kv_heads, int32_t head_dim, int32_t num_pages,
                             float sm_scale, int32_t split_chunk, void *workspace,
                             size_t workspace_bytes, const void *k_new, const void *v_new,
-                            int32_t *dev_error, void *stream) {
+                            int32_t *dev_error, void *stream, int32_t test_skip_page = -1) {
   int32_t st = check_attention_shape(num_qo_heads, num_kv_heads, head_dim);
   if (st != K16V8_OK) return st;
   if (batch < 0 || max_seq_len < 0 || num_pages <= 0 || max_pages_per_seq < 0)
@@ -382,7 +392,7 @@ static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v
       static_cast<__half *>(const_cast<void *>(k_cache)), const_cast<uint8_t *>(v_cache), v_scale,
       block_table, max_pages_per_seq, seq_lens, num_qo_heads, num_kv_heads, num_pages, sm_scale,
       split_chunk, w.chunks, po, pl, static_cast<const __half *>(k_new),
-      static_cast<const __half *>(v_new), dev_error);
+      static_cast<const __half *>(v_new), dev_error, test_skip_page);
 }
 
 extern "C" int32_t k16v8_paged_decode_split(
@@ -395,6 +405,18 @@ extern "C" int32_t k16v8_paged_decode_split(
                              seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim,
                              num_pages, sm_scale, split_chunk, workspace, workspace_bytes, nullptr,
                              nullptr, dev_error, stream);
+}
+
+extern "C" int32_t k16v8_paged_decode_split_wait_test(
+    const void *q, const void *k_cache, const uint8_t *v_cache, const float *v_scale,
+    const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+    int32_t max_seq_len, int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_pages, float sm_scale, int32_t split_chunk, void *workspace,
+    size_t workspace_bytes, int32_t *dev_error, void *stream) {
+  return launch_split<false>(q, k_cache, v_cache, v_scale, block_table, max_pages_per_seq,
+                             seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim,
+                             num_pages, sm_scale, split_chunk, workspace, workspace_bytes, nullptr,
+                             nullptr, dev_error, stream, /*test_skip_page=*/0);
 }
 
 extern "C" int32_t k16v8_paged_decode_append_split(
@@ -544,11 +566,18 @@ extern "C" int32_t k16v8_paged_decode_attention_static(
     float *lse, int32_t *dev_error, void *stream) {
   const int32_t st0 = check_attention_shape(num_qo_heads, num_kv_heads, head_dim);
   if (st0 != K16V8_OK) return st0;
+  // An empty batch needs no scratch: validate it exactly as the workspace
+  // call does (which launches nothing for it).
+  if (batch == 0)
+    return k16v8_paged_decode_attention(q, k_cache, v_cache, v_scale, block_table,
+                                        max_pages_per_seq, seq_lens, max_seq_len, batch,
+                                        num_qo_heads, num_kv_heads, head_dim, num_pages,
+                                        sm_scale, split_chunk, nullptr, 0, out, lse, dev_error,
+                                        stream);
   const size_t need =
       k16v8_decode_workspace_size(batch, num_qo_heads, head_dim, max_seq_len, split_chunk);
   if (need == 0) return K16V8_ERR_INVALID_ARG;
   if (need > K16V8_STATIC_SCRATCH_BYTES) return K16V8_ERR_STATIC_SCRATCH_LIMIT;
-  if (batch == 0) return K16V8_OK;
   void *scratch = nullptr;
   const int32_t st = static_scratch_address(&scratch);
   if (st != K16V8_OK) return st;

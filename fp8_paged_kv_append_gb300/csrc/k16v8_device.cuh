@@ -66,11 +66,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i)
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint32_t max_polls = kMaxPolls) {
+  for (uint32_t i = 0; i < max_polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+
+// Poll limit of the one wait that the bounded-wait test hooks make expire
+// (a copy that is deliberately never issued): short, so the error path is
+// reached at once.
+constexpr uint32_t kTestPolls = 64;
+constexpr uint32_t kTestSpins = 1u << 12;  // the same for a spinning (test_wait) role
 
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
@@ -101,8 +108,9 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
 // Bounded spin on test_wait (no suspension): for waits on the critical path
 // of a pipeline.  The bound is far beyond any real copy or MMA.
 constexpr uint32_t kMaxSpins = 1u << 28;
-__device__ __forceinline__ bool mbar_spin_bounded(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kMaxSpins; ++i)
+__device__ __forceinline__ bool mbar_spin_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint32_t max_spins = kMaxSpins) {
+  for (uint32_t i = 0; i < max_spins; ++i)
     if (mbar_test_wait(bar, parity)) return true;
   return false;
 }

@@ -91,18 +91,27 @@ enum {
   kBarSFull = 13,   // +tile
   kBarPFull = 15,   // +tile, 128 arrivals
   kBarODone = 17,   // +tile
-  kNumBars = 19
+  kBarDrain = 19,   // every MMA of the CTA complete (one commit at the end)
+  kNumBars = 20
 };
 
 // Bounded wait shared by every role.  A wait that runs out sets the
-// CTA-wide abort flag (and the device error word); later waits return at
-// once, so every role runs to the end of its loop.
+// CTA-wide abort flag (and the device error word).  Every wait also gives up
+// as soon as it sees that flag (checked every 1024 polls), and every role
+// leaves its loop when a wait fails, so once one role has given up the
+// others follow within a few polls.  `limit` (0: the default bound) is
+// shortened only by the bounded-wait test hook.
 __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                         int32_t *dev_error, bool spin = false) {
+                                         int32_t *dev_error, bool spin = false,
+                                         uint32_t limit = 0) {
   if (*abort_flag) return false;
   // The single-thread MMA and load roles spin (no suspension, so a hand-off
   // is seen at once); the many-thread roles suspend between polls.
-  if (spin ? mbar_spin_bounded(bar, parity) : mbar_wait_bounded(bar, parity)) return true;
+  const uint32_t n = limit ? limit : (spin ? kMaxSpins : kMaxPolls);
+  for (uint32_t i = 0; i < n; ++i) {
+    if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023u) == 1023u && *abort_flag) return false;
+  }
   *abort_flag = 1;
   flag_error(dev_error, K16V8_DEVERR_TIMEOUT);
   return false;
@@ -120,6 +129,7 @@ __device__ __forceinline__ bool wait_all3(uint64_t *a, uint32_t pa, uint64_t *b,
     if (!dc) dc = mbar_test_wait(c, pc);
     if (!da) da = mbar_test_wait(a, pa);
     if (da && db && dc) return true;
+    if ((i & 1023u) == 1023u && *abort_flag) return false;
   }
   *abort_flag = 1;
   flag_error(dev_error, K16V8_DEVERR_TIMEOUT);
@@ -138,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const int32_t *__restrict__ seq_lens, int32_t total_q, int32_t hq, int32_t hkv,
     int32_t num_pages, float sm_scale, __half *__restrict__ out, float *__restrict__ lse_out,
     int32_t *dev_error, int32_t kv_parts, uint4 *__restrict__ part_o,
-    float *__restrict__ part_lse, int32_t *__restrict__ counters) {
+    float *__restrict__ part_lse, int32_t *__restrict__ counters, int32_t test_withhold) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *base = smem_raw;
   uint8_t *sQ = base + kOffQ;
@@ -183,6 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   const int kv0 = part * n_all / live_parts;
   const int n_kv = (part + 1) * n_all / live_parts - kv0;
   const int32_t *bt = block_table + static_cast<int64_t>(b) * maxp + kv0 * kPagesPerTile;
+  // Bounded-wait test hook (test_withhold != 0, never in production calls):
+  // the first CTA withholds the copies of its first KV tile -- no arrival,
+  // nothing in flight -- so the MMA thread's wait for that tile expires
+  // after kTestSpins polls and every role takes the abort path.
+  const bool withheld = test_withhold != 0 && (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
 
   if (warp == kLoadWarp && lane == 0) {
     // The query load depends on nothing else: start it before the rest of
@@ -244,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const uint32_t tO = tmem + 256 + w * 128;
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < n_kv; ++j) {
-      cta_wait(&bars[kBarSFull + w], j & 1, abort_flag, dev_error);
+      if (!__all_sync(0xffffffffu, cta_wait(&bars[kBarSFull + w], j & 1, abort_flag, dev_error)))
+        break;
       tc::fence_after_sync();
       const bool need_mask = (kv0 + j) * kKv + kKv - 1 > p_lo;  // diagonal tile
       const int lim = p_r - (kv0 + j) * kKv;  // last visible column of this tile
@@ -281,7 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       // PV_w(j-1) and MMAs complete in order, so that is already so; the
       // wait (free by now) only orders the O accesses of a rescale.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        cta_wait(&bars[kBarODone + w], (j - 1) & 1, abort_flag, dev_error);
+        if (!__all_sync(0xffffffffu,
+                        cta_wait(&bars[kBarODone + w], (j - 1) & 1, abort_flag, dev_error)))
+          break;
         tc::fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -335,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     // by row so the next sequence's rows stay untouched.
     const bool full_tile = t_lo + (w + 1) * kQTok <= qlen;  // uniform over the group
     uint8_t *stage = sQ + w * kQBytes;
-    const bool o_ready = cta_wait(&bars[kBarODone + w], (n_kv - 1) & 1, abort_flag, dev_error);
+    const bool o_ready = __all_sync(
+        0xffffffffu, cta_wait(&bars[kBarODone + w], (n_kv - 1) & 1, abort_flag, dev_error));
     bool write_out = true;
     if constexpr (!kSplit) {
       if (o_ready) {
@@ -488,8 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const int dt = tid - 8 * 32;  // 0 .. 32 * kDequantWarps - 1
     for (int j = 0; j < n_kv; ++j) {
       const int s = j & 1;
-      cta_wait(&bars[kBarVstFull + s], (j >> 1) & 1, abort_flag, dev_error);
-      if (j >= 2) cta_wait(&bars[kBarVEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error);
+      if (!cta_wait(&bars[kBarVstFull + s], (j >> 1) & 1, abort_flag, dev_error)) break;
+      if (j >= 2 && !cta_wait(&bars[kBarVEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error))
+        break;
       const uint8_t *vst = sVst + s * kVstStage;
       uint8_t *vdst = sV + s * kVStage;
 #pragma unroll 2
@@ -525,12 +545,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     // (page ids were staged before the set-up barrier)
     // Per tile, lane i < 8 issues the three copies of page i; lane 0 first
     // posts the tile's byte count on both barriers.
+    // last tile issued on each stage: a stage is refilled only after its
+    // previous tile was consumed, so at most that one copy is outstanding
+    int last0 = -1, last1 = -1;
     for (int j = 0; j < n_kv; ++j) {
       const int s = j & 1;
       if (j >= 2) {
-        cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
-        cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
+        const bool ok =
+            cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true) &&
+            cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
+        if (!__all_sync(0xffffffffu, ok)) break;  // stop issuing; drain below
       }
+      if (withheld && j == 0) continue;
+      if (s) last1 = j; else last0 = j;
       const int live = min(kPagesPerTile, (L - (kv0 + j) * kKv + kPage - 1) / kPage);
       int pid = -1;
       if (lane < live) {
@@ -562,11 +589,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       }
     }
     if (lane == 0) {
-      // let the last copies land before shared memory is released (at once
-      // on the normal path, where every copy has been consumed)
-      for (int j = max(0, n_kv - 2); j < n_kv; ++j) {
-        mbar_wait_bounded(&bars[kBarKFull + (j & 1)], (j >> 1) & 1);
-        mbar_wait_bounded(&bars[kBarVstFull + (j & 1)], (j >> 1) & 1);
+      // let the copies issued last on each stage land before shared memory
+      // is released (at once on the normal path, where every copy has been
+      // consumed); nothing else can be outstanding
+      if (last0 >= 0) {
+        mbar_wait_bounded(&bars[kBarKFull], (last0 >> 1) & 1);
+        mbar_wait_bounded(&bars[kBarVstFull], (last0 >> 1) & 1);
+      }
+      if (last1 >= 0) {
+        mbar_wait_bounded(&bars[kBarKFull + 1], (last1 >> 1) & 1);
+        mbar_wait_bounded(&bars[kBarVstFull + 1], (last1 >> 1) & 1);
       }
     }
     __syncwarp();
@@ -608,36 +640,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                          acc0 || kk > 0);
         tc::mma_commit(&bars[kBarODone + w]);
       };
-      cta_wait(&bars[kBarQ], 0, abort_flag, dev_error, true);
-      cta_wait(&bars[kBarKFull], 0, abort_flag, dev_error, true);
-      tc::fence_after_sync();
-      issue_s(0, 0);
-      issue_s(1, 0);
-      tc::mma_commit(&bars[kBarKEmpty]);
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j & 1;
-        const bool more = j + 1 < n_kv;
-        // P_A(j), V(j) and K(j+1) in one polling loop: V and K are nearly
-        // always in place before P_A, so once P_A lands the two MMA groups
-        // go out back to back, with no wait between them.
-        wait_all3(&bars[kBarPFull + 0], j & 1, &bars[kBarVFull + s], (j >> 1) & 1,
-                  more ? &bars[kBarKFull + ((j + 1) & 1)] : nullptr, ((j + 1) >> 1) & 1,
-                  abort_flag, dev_error);
+      const bool started =
+          cta_wait(&bars[kBarQ], 0, abort_flag, dev_error, true) &&
+          cta_wait(&bars[kBarKFull], 0, abort_flag, dev_error, true, withheld ? kTestSpins : 0);
+      if (started) {
         tc::fence_after_sync();
-        issue_pv(0, j);
-        if (more) issue_s(0, j + 1);
-        cta_wait(&bars[kBarPFull + 1], j & 1, abort_flag, dev_error, true);
-        tc::fence_after_sync();
-        issue_pv(1, j);
-        tc::mma_commit(&bars[kBarVEmpty + s]);
-        if (more) {
-          issue_s(1, j + 1);
-          tc::mma_commit(&bars[kBarKEmpty + ((j + 1) & 1)]);
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc::mma_commit(&bars[kBarKEmpty]);
+        for (int j = 0; j < n_kv; ++j) {
+          const int s = j & 1;
+          const bool more = j + 1 < n_kv;
+          // P_A(j), V(j) and K(j+1) in one polling loop: V and K are nearly
+          // always in place before P_A, so once P_A lands the two MMA groups
+          // go out back to back, with no wait between them.
+          if (!wait_all3(&bars[kBarPFull + 0], j & 1, &bars[kBarVFull + s], (j >> 1) & 1,
+                         more ? &bars[kBarKFull + ((j + 1) & 1)] : nullptr, ((j + 1) >> 1) & 1,
+                         abort_flag, dev_error))
+            break;
+          tc::fence_after_sync();
+          issue_pv(0, j);
+          if (more) issue_s(0, j + 1);
+          if (!cta_wait(&bars[kBarPFull + 1], j & 1, abort_flag, dev_error, true)) break;
+          tc::fence_after_sync();
+          issue_pv(1, j);
+          tc::mma_commit(&bars[kBarVEmpty + s]);
+          if (more) {
+            issue_s(1, j + 1);
+            tc::mma_commit(&bars[kBarKEmpty + ((j + 1) & 1)]);
+          }
         }
       }
-      // let every MMA land before tensor memory is released
-      mbar_wait_bounded(&bars[kBarODone + 0], (n_kv - 1) & 1);
-      mbar_wait_bounded(&bars[kBarODone + 1], (n_kv - 1) & 1);
+      // let every MMA this thread issued land before tensor memory is
+      // released: a commit tracks all of them (none: it completes at once)
+      tc::mma_commit(&bars[kBarDrain]);
+      mbar_wait_bounded(&bars[kBarDrain], 0);
+      // and the query copy, which an abort before its wait would leave behind
+      mbar_wait_bounded(&bars[kBarQ], 0);
     }
     __syncwarp();
   }
@@ -735,7 +774,7 @@ static int32_t prefill_launch(
     int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, void *out,
     float *lse, int32_t *dev_error, void *stream, int32_t kv_splits, int32_t max_seq_len,
-    void *workspace, size_t workspace_bytes) {
+    void *workspace, size_t workspace_bytes, int32_t test_withhold = 0) {
   if (num_qo_heads <= 0 || num_kv_heads <= 0) return K16V8_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || num_qo_heads != kGroup * num_kv_heads)
     return K16V8_ERR_UNSUPPORTED_SHAPE;
@@ -812,7 +851,7 @@ static int32_t prefill_launch(
       static_cast<int32_t>(w.parts),
       w.parts > 1 ? reinterpret_cast<uint4 *>(ws + w.o_off) : nullptr,
       w.parts > 1 ? reinterpret_cast<float *>(ws + w.lse_off) : nullptr,
-      w.parts > 1 ? reinterpret_cast<int32_t *>(ws + w.counters_off) : nullptr);
+      w.parts > 1 ? reinterpret_cast<int32_t *>(ws + w.counters_off) : nullptr, test_withhold);
 }
 
 extern "C" int32_t k16v8_paged_prefill_attention(
@@ -824,6 +863,18 @@ extern "C" int32_t k16v8_paged_prefill_attention(
   return prefill_launch(q, qo_indptr, total_q, max_qlen, k_cache, v_cache, v_scale, block_table,
                         max_pages_per_seq, seq_lens, batch, num_qo_heads, num_kv_heads, head_dim,
                         num_pages, sm_scale, out, lse, dev_error, stream, 1, 0, nullptr, 0);
+}
+
+extern "C" int32_t k16v8_paged_prefill_attention_wait_test(
+    const void *q, const int32_t *qo_indptr, int32_t total_q, int32_t max_qlen,
+    const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
+    int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, void *out,
+    float *lse, int32_t *dev_error, void *stream) {
+  return prefill_launch(q, qo_indptr, total_q, max_qlen, k_cache, v_cache, v_scale, block_table,
+                        max_pages_per_seq, seq_lens, batch, num_qo_heads, num_kv_heads, head_dim,
+                        num_pages, sm_scale, out, lse, dev_error, stream, 1, 0, nullptr, 0,
+                        /*test_withhold=*/1);
 }
 
 extern "C" size_t k16v8_prefill_workspace_size(int32_t max_qlen, int32_t batch,

@@ -109,36 +109,49 @@ class MultiLayerDecode:
         self.graph = None
 
     def layer(self, li, q, k_new, v_new, out, lse=None):
+        self.split(li, q, k_new, v_new, out, lse)
+        self.merge(li, out, lse)
+
+    def split(self, li, q, k_new, v_new, out, lse=None, append=True):
+        """Layer li's launches up to the attention split (the separate append
+        first, unless the split kernel does it or append is False)."""
         if self.schedule == "balanced_fused":
             K.k16v8_paged_decode_append_balanced_split(
                 q, k_new, v_new, self.k_caches[li], self.v_caches[li], self.v_scales[li],
                 self.block_table, self.seq_lens, self.sm_scale, self.workspace, out, lse,
                 self.dev_error, flags=K.DECODE_METADATA_READY)
-            K.k16v8_merge_balanced(self.workspace, self.hkv, out, lse)
-            return
-        if self.schedule == "fused":
+        elif self.schedule == "fused":
             K.k16v8_paged_decode_append_split(
                 q, k_new, v_new, self.k_caches[li], self.v_caches[li], self.v_scales[li],
                 self.block_table, self.seq_lens, self.max_seq_len, self.sm_scale, self.chunk,
                 self.workspace, self.dev_error)
+        else:
+            if append:
+                K.k16v8_kv_append(k_new, v_new, self.slots, self.v_scales[li],
+                                  self.k_caches[li], self.v_caches[li], self.dev_error)
+            if self.schedule == "balanced":
+                K.k16v8_paged_decode_balanced_split(q, self.k_caches[li], self.v_caches[li],
+                                                    self.v_scales[li], self.block_table,
+                                                    self.seq_lens, self.sm_scale, self.workspace,
+                                                    out, lse, self.dev_error,
+                                                    flags=K.DECODE_METADATA_READY)
+            else:
+                K.k16v8_paged_decode_split(q, self.k_caches[li], self.v_caches[li],
+                                           self.v_scales[li], self.block_table, self.seq_lens,
+                                           self.max_seq_len, self.sm_scale, self.chunk,
+                                           self.workspace, self.dev_error)
+
+    def merge(self, li, out, lse=None):
+        """Layer li's merge of the split partials into out / lse."""
+        if self.schedule in ("balanced", "balanced_fused"):
+            K.k16v8_merge_balanced(self.workspace, self.hkv, out, lse)
+        else:
             K.k16v8_merge_states(self.partial_o, self.partial_lse, self.seq_lens, self.chunk,
                                  out, lse)
-            return
-        K.k16v8_kv_append(k_new, v_new, self.slots, self.v_scales[li], self.k_caches[li],
-                          self.v_caches[li], self.dev_error)
-        if self.schedule == "balanced":
-            K.k16v8_paged_decode_balanced_split(q, self.k_caches[li], self.v_caches[li],
-                                                self.v_scales[li], self.block_table,
-                                                self.seq_lens, self.sm_scale, self.workspace,
-                                                out, lse, self.dev_error,
-                                                flags=K.DECODE_METADATA_READY)
-            K.k16v8_merge_balanced(self.workspace, self.hkv, out, lse)
-            return
-        K.k16v8_paged_decode_split(q, self.k_caches[li], self.v_caches[li], self.v_scales[li],
-                                   self.block_table, self.seq_lens, self.max_seq_len,
-                                   self.sm_scale, self.chunk, self.workspace, self.dev_error)
-        K.k16v8_merge_states(self.partial_o, self.partial_lse, self.seq_lens, self.chunk, out,
-                             lse)
+
+    def launches_per_layer(self) -> int:
+        """Launches per layer: 2 when the append runs inside the split."""
+        return 2 if self.schedule in ("fused", "balanced_fused") else 3
 
     def step(self, qs, k_news, v_news, outs, lses=None):
         for li in range(self.layers):

@@ -85,6 +85,12 @@ SIGNATURES = {
                                                             _P, _i32, _i32, _i32, _i32, _i32,
                                                             _f32, _P, _sz, _P, _P, _i32, _P,
                                                             _P]),
+    "k16v8_paged_decode_split_wait_test": (_i32, [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32,
+                                                  _i32, _i32, _i32, _i32, _f32, _i32, _P, _sz,
+                                                  _P, _P]),
+    "k16v8_paged_prefill_attention_wait_test": (_i32, [_P, _P, _i32, _i32, _P, _P, _P, _P,
+                                                       _i32, _P, _i32, _i32, _i32, _i32, _i32,
+                                                       _f32, _P, _P, _P, _P]),
     "k16v8_read_device_error": (_i32, [_P, _P, ctypes.POINTER(_i32)]),
     "k16v8_status_string": (ctypes.c_char_p, [_i32]),
 }
@@ -197,6 +203,20 @@ def k16v8_paged_decode_split(q, k_cache, v_cache, v_scale, block_table, seq_lens
     _check("k16v8_paged_decode_split", st)
 
 
+def k16v8_paged_decode_split_wait_test(q, k_cache, v_cache, v_scale, block_table, seq_lens,
+                                       max_seq_len, sm_scale, split_chunk, workspace,
+                                       dev_error=None, stream=None):
+    """Test hook: k16v8_paged_decode_split with one page copy of the first CTA
+    withheld, so that CTA's bounded wait expires (K16V8_DEVERR_TIMEOUT)."""
+    B, hq, d = q.shape
+    st = load_library().k16v8_paged_decode_split_wait_test(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), int(max_seq_len), B, hq, k_cache.shape[1], d,
+        k_cache.shape[0], float(sm_scale), int(split_chunk), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_decode_split_wait_test", st)
+
+
 def k16v8_merge_states(partial_o, partial_lse, seq_lens, split_chunk, out, lse=None,
                        stream=None):
     B, hq, C, d = partial_o.shape
@@ -293,6 +313,21 @@ def k16v8_paged_prefill_attention(q, qo_indptr, max_qlen, k_cache, v_cache, v_sc
         seq_lens.shape[0], hq, k_cache.shape[1], d, k_cache.shape[0], float(sm_scale), _ptr(out),
         _ptr(lse), _ptr(dev_error), _stream(stream))
     _check("k16v8_paged_prefill_attention", st)
+
+
+def k16v8_paged_prefill_attention_wait_test(q, qo_indptr, max_qlen, k_cache, v_cache, v_scale,
+                                            block_table, seq_lens, sm_scale, out, lse=None,
+                                            dev_error=None, stream=None):
+    """Test hook: k16v8_paged_prefill_attention with the first KV tile of the
+    first CTA withheld, so that CTA's bounded wait expires
+    (K16V8_DEVERR_TIMEOUT)."""
+    total_q, hq, d = q.shape
+    st = load_library().k16v8_paged_prefill_attention_wait_test(
+        _ptr(q), _ptr(qo_indptr), total_q, int(max_qlen), _ptr(k_cache), _ptr(v_cache),
+        _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        seq_lens.shape[0], hq, k_cache.shape[1], d, k_cache.shape[0], float(sm_scale), _ptr(out),
+        _ptr(lse), _ptr(dev_error), _stream(stream))
+    _check("k16v8_paged_prefill_attention_wait_test", st)
 
 
 def k16v8_prefill_workspace_size(max_qlen, batch, num_qo_heads, num_kv_heads, head_dim,

@@ -465,6 +465,46 @@ int32_t k16v8_paged_decode_attention_static(
     float *lse, int32_t *dev_error, void *stream);
 
 /*
+ * Test hooks of the bounded waits.  Every wait of a k16v8 kernel on an
+ * asynchronous copy or a hand-off between warp roles gives up after a
+ * bounded number of polls, sets K16V8_DEVERR_TIMEOUT in the error word,
+ * lets the copies and tensor-core operations it did issue complete, and
+ * returns, so a lost hand-off never hangs the GPU and the stream stays
+ * usable.  The page records failures rather than hiding them ("Fixed
+ * throughput studies"); these two calls let a test reach that path without
+ * any fault: each runs the named call with the same arguments, except that
+ * the first CTA of the grid withholds one copy (issues nothing and arrives
+ * nowhere for it) and waits for it with a short limit.
+ *   k16v8_paged_decode_split_wait_test: as k16v8_paged_decode_split; warp
+ *     0 of CTA (chunk 0, KV head 0, sequence 0) withholds its first page.
+ *   k16v8_paged_prefill_attention_wait_test: as
+ *     k16v8_paged_prefill_attention; CTA (0, 0, 0) (the last query-tile
+ *     pair of sequence 0, KV head 0) withholds its first KV tile.
+ * The withholding CTA's results are incomplete (its partial, or its output
+ * rows, are not valid); every other CTA computes normally.  After the call
+ * the error word holds K16V8_DEVERR_TIMEOUT (if that CTA had work) and
+ * later calls on the stream run normally.  Not for production use.
+ */
+int32_t k16v8_paged_decode_split_wait_test(const void *q, const void *k_cache,
+                                           const uint8_t *v_cache, const float *v_scale,
+                                           const int32_t *block_table,
+                                           int32_t max_pages_per_seq,
+                                           const int32_t *seq_lens, int32_t max_seq_len,
+                                           int32_t batch, int32_t num_qo_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t num_pages, float sm_scale,
+                                           int32_t split_chunk, void *workspace,
+                                           size_t workspace_bytes, int32_t *dev_error,
+                                           void *stream);
+
+int32_t k16v8_paged_prefill_attention_wait_test(
+    const void *q, const int32_t *qo_indptr, int32_t total_q, int32_t max_qlen,
+    const void *k_cache, const uint8_t *v_cache, const float *v_scale, const int32_t *block_table,
+    int32_t max_pages_per_seq, const int32_t *seq_lens, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_pages, float sm_scale, void *out,
+    float *lse, int32_t *dev_error, void *stream);
+
+/*
  * Wait for `stream`, then copy the device error word to *host_value and
  * return K16V8_OK when it is zero, K16V8_ERR_DEVICE_BOUNDS otherwise
  * (K16V8_ERR_CUDA if the synchronisation or copy fails).

@@ -26,13 +26,37 @@ def test_reference_arm_prints_contract_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
 
-    # same metric and config as the GPU arm's default line
+    # same metric and config as the GPU arm's default line (the 40-layer full pool)
     sys.path.insert(0, ROOT)
     import bench
-    w, label, chunk = bench.make_workload("1k")
+    from fp8_paged_kv_append_gb300 import workloads
+    lay = workloads.fullpool_layout(seed=bench.FULLPOOL_SEED)
     assert d["metric"] == bench.METRIC
-    assert d["config"] == bench.config_of(w, label, chunk, bench.replicas_for(w),
-                                          bench.DEFAULT_DECODE)
+    assert d["config"] == bench.fullpool_config(lay, 40, "auto")
+    assert d["config"]["layers"] == 40 and d["config"]["batch"] == 64
+
+
+def test_reference_arm_one_layer_workload_config():
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse_args(["--impl", "reference", "--workload", "1k"])
+    w, chunk, sample, desc, config = bench.reference_workload(args)
+    assert config == bench.config_of(w, "decode 1K/batch 32", 384, bench.replicas_for(w),
+                                     bench.DEFAULT_DECODE)
+    assert len(sample) == 2
+
+
+def test_fullpool_cpu_sample_spans_the_length_range():
+    sys.path.insert(0, ROOT)
+    import bench
+    from fp8_paged_kv_append_gb300 import workloads
+    lay = workloads.fullpool_layout(seed=bench.FULLPOOL_SEED)
+    w, desc = bench.fullpool_cpu_sample()
+    assert w.batch == 8
+    assert int(w.seq_lens.min()) == int(lay.seq_lens.min())
+    assert int(w.seq_lens.max()) == int(lay.seq_lens.max())
+    assert set(w.seq_lens.tolist()) <= set(lay.seq_lens.tolist())
+    assert (w.num_qo_heads, w.num_kv_heads, w.head_dim) == (40, 10, 128)
 
 
 def test_replicas_cover_four_l2():

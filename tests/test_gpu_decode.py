@@ -155,3 +155,45 @@ def test_merge_indexing_bit_exact(K):
     K.k16v8_merge_states(to_dev(po), to_dev(pl), to_dev(lens), chunk, out, lse)
     ro, rl = oracle.merge(po.astype(np.float64), pl.astype(np.float64), nc)
     check_close(out.float().cpu().numpy(), ro, lse.cpu().numpy(), rl)
+
+
+def _page_sum_stress(seed):
+    """Near-uniform scores (queries scaled down to |s| < ~0.1) over values
+    that all quantise to the extreme codes +-448: every per-page product sum
+    the kernels accumulate in fp16 runs up to 16 x 448 = 7,168, where an fp16
+    ulp is 4.  Even KV heads hold +v only (no cancellation: the largest
+    sums), odd heads random signs.  Lengths 1, 16, 17 and 8,192."""
+    w = workloads.make_decode("page-sum stress", seed, [1, 16, 17, 8192])
+    rng = np.random.Generator(np.random.PCG64(seed + 1))
+    w.q = (w.q.astype(np.float32) * np.float32(0.02)).astype(np.float16)
+    sign = np.where(rng.integers(0, 2, w.v_tok.shape) == 1, 1.0, -1.0).astype(np.float32)
+    sign[:, 0::2, :] = 1.0
+    w.v_tok = (sign * np.float32(0.75)).astype(np.float16)
+    w.v_scale = workloads.calibrate_v_scale(w.v_tok)
+    return w
+
+
+@pytest.mark.parametrize("chunk", [16, 512])
+def test_decode_fp16_page_sums_at_code_448(K, chunk):
+    w = _page_sum_stress(21)
+    okc, ovc = oracle_cache(w)
+    assert set(np.unique(ovc).tolist()) <= {0x7E, 0xFE}  # +-448 only
+    compare_workload(K, w, chunk)
+
+
+def test_decode_balanced_fp16_page_sums_at_code_448(K):
+    w = _page_sum_stress(22)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    kc, vc = gpu_cache(w, K, err)
+    okc, ovc = oracle_cache(w)
+    B, hq, d = w.q.shape
+    ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d), dtype=torch.uint8,
+                     device=dev())
+    out = torch.empty((B, hq, d), dtype=torch.float16, device=dev())
+    lse = torch.empty((B, hq), dtype=torch.float32, device=dev())
+    K.k16v8_paged_decode_attention_balanced(to_dev(w.q), kc, vc, to_dev(w.v_scale),
+                                            to_dev(w.block_table), to_dev(w.seq_lens),
+                                            w.sm_scale, ws, out, lse, err)
+    assert K.k16v8_read_device_error(err) == 0
+    ref = oracle.paged_decode(w.q, okc, ovc, w.v_scale, w.block_table, w.seq_lens, w.sm_scale)
+    check_close(out.float().cpu().numpy(), ref["out"], lse.cpu().numpy(), ref["lse"])

@@ -55,12 +55,14 @@ def run_calls(K, p, rows_to_check=None, err=None, kv_splits=None, max_seq_len_hi
     return res
 
 
-def check_against_oracle(p, res, sample=None):
+def check_against_oracle(p, res, sample=None, full_calls=()):
+    """Every call against the oracle: all rows, or every `sample`-th row plus
+    each sequence's last row (all rows of the calls in full_calls)."""
     okc, ovc = oracle_cache(p)
     for ci, call in enumerate(p.calls):
         o, l = res[ci]
         rows = None
-        if sample is not None:
+        if sample is not None and ci not in full_calls:
             rows = np.unique(np.concatenate([np.arange(0, len(call.rows), sample),
                                              call.qo_indptr[1:] - 1])).astype(np.int64)
         ro, rl = oracle.paged_prefill(np.ascontiguousarray(p.q[call.rows]), call.qo_indptr, okc,
@@ -94,10 +96,28 @@ def test_prefill_8x1k(K):
     check_against_oracle(p, res)
 
 
-def test_prefill_1x8k_in_8_chunks_sampled(K):
+def test_prefill_1x8k_in_8_chunks_last_chunk_complete(K):
+    """The 8192-token prompt in 8 chunks: every row of the last chunk (prefix
+    7,169..8,192 positions), every 41st row of the others."""
     p = workloads.prefill_1x8k()
     res = run_calls(K, p)
-    check_against_oracle(p, res, sample=41)
+    check_against_oracle(p, res, sample=41, full_calls=(len(p.calls) - 1,))
+
+
+@pytest.mark.parametrize("kv_splits", [None, 4])
+def test_prefill_prefix_beyond_staged_page_ids(K, kv_splits):
+    """A 9,000-token prompt in chunks of 1,024: the last chunk's query-tile
+    pairs see up to 563 pages, more than the kernel stages in shared memory
+    (512), so the plain call reads the rest of the page ids from the block
+    table in global memory.  Every row of the last chunk is checked; the
+    KV-split form (4 parts) runs the same calls with short parts."""
+    p = workloads.make_prefill("beyond ids", 12, [9000], chunk=1024, num_qo_heads=8,
+                               num_kv_heads=2)
+    assert -(-9000 // 16) > 512
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    res = run_calls(K, p, err=err, kv_splits=kv_splits)
+    assert K.k16v8_read_device_error(err) == 0
+    check_against_oracle(p, res, sample=29, full_calls=(len(p.calls) - 1,))
 
 
 def test_prefill_bad_page_is_flagged(K):
@@ -137,7 +157,7 @@ def test_prefill_1x8k_kv_split_auto_sampled(K):
     err = torch.zeros(1, dtype=torch.int32, device=dev())
     res = run_calls(K, p, err=err, kv_splits=0)
     assert K.k16v8_read_device_error(err) == 0
-    check_against_oracle(p, res, sample=41)
+    check_against_oracle(p, res, sample=41, full_calls=(len(p.calls) - 1,))
     res2 = run_calls(K, p, err=err, kv_splits=0, max_seq_len_hint=True)
     assert K.k16v8_read_device_error(err) == 0
     check_against_oracle(p, res2, sample=41)
