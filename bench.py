@@ -831,10 +831,15 @@ class FullPoolBench:
         different pool each), replayed `reps` times between CUDA events on
         the launching stream."""
         torch, s = self.torch, self.step
+        # The layers share one workspace, so back-to-back splits leave only the
+        # last layer's partials for the merges: they write scratch outputs,
+        # never the step's.
+        so = [torch.empty_like(o) for o in self.outs]
+        sl = [torch.empty_like(x) for x in self.lses]
         res = []
-        for fn in (lambda li: s.split(li, self.qs[li], self.kn[li], self.vn[li], self.outs[li],
-                                      self.lses[li], append=False),
-                   lambda li: s.merge(li, self.outs[li], self.lses[li])):
+        for fn in (lambda li: s.split(li, self.qs[li], self.kn[li], self.vn[li], so[li], sl[li],
+                                      append=False),
+                   lambda li: s.merge(li, so[li], sl[li])):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=torch.cuda.Stream(self.dev),
                                   capture_error_mode="thread_local"):
