@@ -149,6 +149,7 @@ KERNEL_PROFILES = {
     ("8k", "chunked"): ("decode_split_8k_b16.md", _DECODE_SRC),
     ("8k", "balanced_fused"): ("decode_balanced_append_8k_b16.md", _BALANCED_SRC),
     ("fullpool", "fused"): ("decode_split_append_fullpool_layer.md", _DECODE_SRC),
+    ("prefill_8x1024", "kv_append"): ("kv_append_8x1024.md", ["kv_append.cu", "k16v8_device.cuh"]),
 }
 
 
@@ -689,7 +690,7 @@ def kv_append_bytes(p) -> int:
     return int(p.q.shape[0]) * p.num_kv_heads * p.head_dim * (2 + 2 + 2 + 1)
 
 
-def prefill_line(p, device, steps, warmup, tensor_peak, hbm_peak):
+def prefill_line(p, device, steps, warmup, tensor_peak, hbm_peak, workload=None):
     """The prefill calls through the KV-split entry point (the library picks
     the parts; 1 when the items fill the GPU), and the plain call beside it
     when the split one split anything.  The cache write of the prompts
@@ -710,7 +711,8 @@ def prefill_line(p, device, steps, warmup, tensor_peak, hbm_peak):
                 "algorithmic_bytes": ab,
                 "achieved": round(ab / (app_ms * 1e-3) / 1e9, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(ab / (app_ms * 1e-3) / 1e9 / hbm_peak, 4),
-                "frac_of_nominal": round(ab / (app_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4)}}
+                "frac_of_nominal": round(ab / (app_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+                "traffic": traffic_from_profiles(workload, "kv_append") if workload else None}}
     if pb.ws_bytes:
         del pb
         plain = PrefillBench(p, device, split=False)
@@ -1242,7 +1244,8 @@ def extra_lines(args, device):
     extra["prefill"] = {
         "peak_tflops": tpeak,
         "peak_kind": f"{peak_kind} dense bf16 (fp16 has the same nominal rate)",
-        "8x1024": prefill_line(workloads.prefill_8x1k(), device, 10, 3, tpeak, hbm_peak),
+        "8x1024": prefill_line(workloads.prefill_8x1k(), device, 10, 3, tpeak, hbm_peak,
+                               "prefill_8x1024"),
         "1x8192_in_8_chunks": prefill_line(workloads.prefill_1x8k(), device, 5, 2, tpeak,
                                            hbm_peak)}
     for name, (wf, lf, cf) in (("decode_1k_b32", (w1, l1, c1)), ("decode_8k_b16", (w8, l8, c8))):
@@ -1355,7 +1358,7 @@ def main_prefill(args):
     K.load_library()
     hbm_peak, tpeak, tkind = load_peaks()
     res = {"8x1024": prefill_line(workloads.prefill_8x1k(), device, args.steps,
-                                  max(3, args.warmup), tpeak, hbm_peak)}
+                                  max(3, args.warmup), tpeak, hbm_peak, "prefill_8x1024")}
     if not args.no_extra:
         res["1x8192_in_8_chunks"] = prefill_line(workloads.prefill_1x8k(), device, args.steps,
                                                  max(3, args.warmup), tpeak, hbm_peak)
