@@ -96,21 +96,29 @@ enum {
 };
 
 // Bounded wait shared by every role.  A wait that runs out sets the
-// CTA-wide abort flag (and the device error word).  Every wait also gives up
-// as soon as it sees that flag (checked every 1024 polls), and every role
-// leaves its loop when a wait fails, so once one role has given up the
-// others follow within a few polls.  `limit` (0: the default bound) is
-// shortened only by the bounded-wait test hook.
+// CTA-wide abort flag (and the device error word); every role leaves its
+// loop when a wait fails, and a wait that starts after the flag is up
+// returns at once.  The suspending waits (softmax, dequant and load warps)
+// also give up as soon as they see the flag (checked every 1024 polls), so
+// once one role has given up the others follow within a few polls.  The
+// MMA thread's spinning waits do not check it: a check in those loops cost
+// the kernel 5% (they share a scheduler with softmax warps), and that
+// thread waits only on the loads and the softmax warps, whose own waits
+// end.  `limit` (0: the default bound) is shortened only by the
+// bounded-wait test hook.
 __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                          int32_t *dev_error, bool spin = false,
                                          uint32_t limit = 0) {
   if (*abort_flag) return false;
-  // The single-thread MMA and load roles spin (no suspension, so a hand-off
-  // is seen at once); the many-thread roles suspend between polls.
-  const uint32_t n = limit ? limit : (spin ? kMaxSpins : kMaxPolls);
-  for (uint32_t i = 0; i < n; ++i) {
-    if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 1023u && *abort_flag) return false;
+  if (spin) {
+    // the MMA thread spins (no suspension, so a hand-off is seen at once)
+    if (mbar_spin_bounded(bar, parity, limit ? limit : kMaxSpins)) return true;
+  } else {
+    const uint32_t n = limit ? limit : kMaxPolls;
+    for (uint32_t i = 0; i < n; ++i) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((i & 1023u) == 1023u && *abort_flag) return false;
+    }
   }
   *abort_flag = 1;
   flag_error(dev_error, K16V8_DEVERR_TIMEOUT);
@@ -129,7 +137,6 @@ __device__ __forceinline__ bool wait_all3(uint64_t *a, uint32_t pa, uint64_t *b,
     if (!dc) dc = mbar_test_wait(c, pc);
     if (!da) da = mbar_test_wait(a, pa);
     if (da && db && dc) return true;
-    if ((i & 1023u) == 1023u && *abort_flag) return false;
   }
   *abort_flag = 1;
   flag_error(dev_error, K16V8_DEVERR_TIMEOUT);
@@ -551,9 +558,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     for (int j = 0; j < n_kv; ++j) {
       const int s = j & 1;
       if (j >= 2) {
+        // suspending waits: the warp runs a tile ahead, and a spinning one
+        // would take issue slots from the softmax warps of its scheduler
         const bool ok =
-            cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true) &&
-            cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error, true);
+            cta_wait(&bars[kBarKEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error) &&
+            cta_wait(&bars[kBarVstEmpty + s], ((j >> 1) - 1) & 1, abort_flag, dev_error);
         if (!__all_sync(0xffffffffu, ok)) break;  // stop issuing; drain below
       }
       if (withheld && j == 0) continue;
