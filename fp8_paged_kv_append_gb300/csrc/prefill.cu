@@ -19,11 +19,12 @@
 //    otherwise the stale max is kept -- exact, as the final normalisation
 //    uses the same max), fp32 row sum, P (fp16) back into tensor memory;
 //    finally O / l * v_scale -> fp16 and the LSE.
-//  * warps 8-11: V dequantisation, E4M3 pages -> fp16 MN-major SW128 tile.
+//  * warps 8, 10, 11: V dequantisation, E4M3 pages -> fp16 MN-major SW128
+//    tile.
 //  * warp 12: loads -- Q by TMA (3-D box: 64 dims x 4 heads x 32 tokens),
 //    K pages by TMA straight into the K-major SW128 operand layout, E4M3 V
 //    pages by bulk copy; two stages each.
-//  * warp 13: one thread issues every tcgen05.mma (kind::f16, fp32
+//  * warp 9: one thread issues every tcgen05.mma (kind::f16, fp32
 //    accumulators): S = Q K^T with both operands in shared memory, O += P V
 //    with P read from tensor memory; order S_A(0) S_B(0) | PV_A(j) S_A(j+1)
 //    PV_B(j) S_B(j+1) ..., so one tile's softmax overlaps the other tile's
@@ -59,9 +60,20 @@ constexpr int kQTok = 32;                   // query tokens per tile
 constexpr int kRows = kQTok * kGroup;       // 128 MMA rows per tile
 constexpr int kKv = 128;                    // KV positions per tile
 constexpr int kPagesPerTile = kKv / kPage;  // 8
-constexpr int kDequantWarps = 4;
-constexpr int kLoadWarp = 12;  // warp 13 issues the MMAs
-constexpr int kThreads = 14 * 32;
+// Warp roles: 0-7 softmax (warp w reads tensor-memory lanes 32(w%4)..+31,
+// so each group of 4 spans the 4 schedulers, warp w on scheduler w%4); 8, 10
+// and 11 dequantise V; 9 issues the MMAs; 12 loads.  The MMA warp is the
+// only non-softmax warp on its scheduler: every tcgen05.mma it issues needs
+// an issue slot there, and a dequant warp beside it (the first layout) cost
+// 2-5% (measured).
+constexpr int kDequantWarps = 3;
+constexpr int kMmaWarp = 9;
+constexpr int kLoadWarp = 12;
+constexpr int kThreads = 13 * 32;
+// Rank of a dequant warp among the dequant warps, or -1.
+__device__ __forceinline__ int dequant_rank(int warp) {
+  return warp == 8 ? 0 : (warp == 10 ? 1 : (warp == 11 ? 2 : -1));
+}
 
 constexpr uint32_t kQBytes = kRows * 256;          // one Q tile: 2 K-blocks [128][64] fp16
 constexpr uint32_t kKBlk = kKv * 128;              // [128 pos][64 dims] fp16
@@ -509,9 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         tc::bulk_wait_read();  // the buffer must outlive the copy's reads
       }
     }
-  } else if (warp < 8 + kDequantWarps) {
+  } else if (dequant_rank(warp) >= 0) {
     // ================= V dequantisation =================
-    const int dt = tid - 8 * 32;  // 0 .. 32 * kDequantWarps - 1
+    const int dt = dequant_rank(warp) * 32 + lane;  // 0 .. 32 * kDequantWarps - 1
     for (int j = 0; j < n_kv; ++j) {
       const int s = j & 1;
       if (!cta_wait(&bars[kBarVstFull + s], (j >> 1) & 1, abort_flag, dev_error)) break;
@@ -520,8 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       const uint8_t *vst = sVst + s * kVstStage;
       uint8_t *vdst = sV + s * kVStage;
 #pragma unroll 2
-      for (int i = 0; i < kKv * 8 / (kDequantWarps * 32); ++i) {
-        const int id = dt + kDequantWarps * 32 * i;  // chunks of 16 E4M3 values
+      for (int id = dt; id < kKv * 8; id += kDequantWarps * 32) {  // chunks of 16 E4M3 values
         const int pos = id >> 3, c16 = id & 7;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if ((kv0 + j) * kKv + pos < L) {
@@ -611,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp == kMmaWarp) {
     // ================= MMA issue =================
     if (lane == 0) {
       constexpr uint32_t kIdescQK = tc::idesc_f16_f32(kRows, kKv, false, false);
