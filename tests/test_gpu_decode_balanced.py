@@ -197,3 +197,46 @@ def test_balanced_host_checks(K):
     assert e.value.status == K.K16V8_ERR_INVALID_ARG
     assert K.k16v8_decode_balanced_workspace_size(8193, hq, d) == 0
     assert K.k16v8_decode_balanced_workspace_size(B, hq, 64) == 0
+
+
+def test_metadata_ready_flag_in_a_graph_is_bit_identical(K):
+    """The decode step as the bench and MultiLayerDecode run it: the fused
+    load-balanced split and its merge captured in one CUDA graph, steps back
+    to back (programmatic launch overlap between them), once with the
+    block table and lengths read before the wait on the preceding kernel
+    (K16V8_DECODE_METADATA_READY) and once without.  Outputs, LSEs and cache
+    bytes must be bit-identical, and match the oracle."""
+    w = workloads.decode_1k_b32()
+    nr = w.new_rows
+    B, hq, d = w.q.shape
+    results = []
+    for flags in (0, K.DECODE_METADATA_READY):
+        kc, vc = gpu_cache(w, K)
+        ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d), dtype=torch.uint8,
+                         device=dev())
+        out = torch.full((B, hq, d), float("nan"), dtype=torch.float16, device=dev())
+        lse = torch.full((B, hq), float("nan"), dtype=torch.float32, device=dev())
+        err = torch.zeros(1, dtype=torch.int32, device=dev())
+        args = (to_dev(w.q), to_dev(w.k_tok[nr]), to_dev(w.v_tok[nr].astype(np.float16)), kc, vc,
+                to_dev(w.v_scale), to_dev(w.block_table), to_dev(w.seq_lens), w.sm_scale, ws)
+
+        def step():
+            K.k16v8_paged_decode_append_balanced_split(*args, out, lse, err, flags=flags)
+            K.k16v8_merge_balanced(ws, w.num_kv_heads, out, lse)
+
+        step()  # eager run configures the kernels
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream(), capture_error_mode="thread_local"):
+            for _ in range(4):
+                step()
+        out.fill_(float("nan"))
+        g.replay()
+        assert K.k16v8_read_device_error(err) == 0
+        results.append((out.clone(), lse.clone(), kc.clone(), vc.clone()))
+    (o0, l0, k0, v0), (o1, l1, k1, v1) = results
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    assert torch.equal(k0.view(torch.int16), k1.view(torch.int16)) and torch.equal(v0, v1)
+    okc, ovc = oracle_cache(w)
+    ref = oracle.paged_decode(w.q, okc, ovc, w.v_scale, w.block_table, w.seq_lens, w.sm_scale)
+    check_close(o1.float().cpu().numpy(), ref["out"], l1.cpu().numpy(), ref["lse"])
