@@ -764,12 +764,13 @@ class FullPoolBench:
     new token's append, split-KV attention, merge), captured as one CUDA
     graph per step by MultiLayerDecode."""
 
-    def __init__(self, device, layers=40, schedule="auto"):
+    def __init__(self, device, layers=40, schedule="auto", split_chunk=512):
         import torch
         from fp8_paged_kv_append_gb300 import k16v8 as K
         from fp8_paged_kv_append_gb300 import workloads
         from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
         self.torch, self.K, self.dev, self.layers = torch, K, device, layers
+        self.split_chunk = split_chunk
         self.MLD = MultiLayerDecode
         self.lay = lay = workloads.fullpool_layout(seed=FULLPOOL_SEED)
         P, B = lay.num_pages, len(lay.seq_lens)
@@ -799,7 +800,7 @@ class FullPoolBench:
     def make_step(self, bt, lens, slots, schedule):
         return self.MLD([p[0] for p in self.pools], [p[1] for p in self.pools],
                         [p[2] for p in self.pools], bt, lens, slots, int(self.L.max()), 40,
-                        split_chunk=512, schedule=schedule)
+                        split_chunk=self.split_chunk, schedule=schedule)
 
     @property
     def kv_bytes_per_layer(self) -> int:
@@ -1139,7 +1140,8 @@ def parse_args(argv=None):
                     help="decode schedule of the main line (default: auto on the full pool, "
                          "balanced_fused on one layer)")
     ap.add_argument("--split-chunk", type=int, default=0,
-                    help="tokens per split-KV chunk of a one-layer workload (0: its default)")
+                    help="tokens per split-KV chunk of the chunked schedules (0: the workload's "
+                         "default)")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the full-pool workload (fewer for profiling captures)")
     args = ap.parse_args(argv)
@@ -1154,7 +1156,8 @@ def measure_fullpool(args, device, rank, world):
     """The headline: the 40-layer decode step over the 32 GiB pool."""
     import torch
     hbm_peak, _, peak_kind = load_peaks()
-    fb = FullPoolBench(device, layers=args.layers, schedule=args.decode)
+    fb = FullPoolBench(device, layers=args.layers, schedule=args.decode,
+                       split_chunk=args.split_chunk or 512)
     warm = max(args.warmup, 3)
     clocks = ClockSampler(device.index or 0).start()
     ms = fb.run(args.steps, warm)
