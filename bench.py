@@ -133,10 +133,10 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-MODES = ("chunked", "fused", "balanced", "balanced_fused")
+MODES = ("chunked", "fused", "balanced", "balanced_fused", "whole")
 DEFAULT_DECODE = "balanced_fused"  # schedule of a one-layer decode line
 SUFFIX = {"chunked": "chunked", "fused": "fused_append", "balanced": "balanced",
-          "balanced_fused": "balanced_fused_append"}
+          "balanced_fused": "balanced_fused_append", "whole": "whole_sequence"}
 
 _DECODE_SRC = ["decode.cu", "decode_page.cuh", "k16v8_device.cuh"]
 _BALANCED_SRC = ["decode_balanced.cu", "decode_page.cuh", "k16v8_device.cuh"]
@@ -197,15 +197,17 @@ class DecodeBench:
     def __init__(self, w, device, split_chunk=512, replicas=None, mode="chunked"):
         """mode: "chunked" (append, split, merge), "fused" (append fused into
         the split kernel, merge), "balanced" (append, load-balanced split,
-        its merge) or "balanced_fused" (append fused into the load-balanced
-        split, its merge)."""
+        its merge), "balanced_fused" (append fused into the load-balanced
+        split, its merge) or "whole" (one CTA per (sequence, KV head) over the
+        whole sequence, append folded in, the output written by that kernel:
+        one launch)."""
         import torch
         from fp8_paged_kv_append_gb300 import k16v8 as K
         assert mode in MODES
         self.K, self.torch, self.w, self.dev = K, torch, w, device
         self.chunk = split_chunk
         self.mode = mode
-        self.fused = mode in ("fused", "balanced_fused")
+        self.fused = mode in ("fused", "balanced_fused", "whole")
         self.balanced = mode in ("balanced", "balanced_fused")
         self.R = replicas or replicas_for(w)
         P = w.num_pages
@@ -232,6 +234,8 @@ class DecodeBench:
         self.q = td(w.q)
         self.seq_lens = td(w.seq_lens)
         self.max_len = int(w.seq_lens.max())
+        if mode == "whole":  # one chunk covering the longest sequence
+            self.chunk = max(16, -(-self.max_len // 16) * 16)
         if self.balanced:
             self.ws = torch.empty(K.k16v8_decode_balanced_workspace_size(B, hq, d),
                                   dtype=torch.uint8, device=device)
@@ -263,7 +267,12 @@ class DecodeBench:
 
     def split(self, i):
         K, r = self.K, i % self.R
-        if self.mode == "fused":
+        if self.mode == "whole":
+            K.k16v8_paged_decode_append_attention(
+                self.q, self.k_new16, self.v_new16, self.kc, self.vc, self.v_scale, self.bt[r],
+                self.seq_lens, self.max_len, self.w.sm_scale, self.chunk, self.ws, self.out,
+                self.lse, self.err)
+        elif self.mode == "fused":
             K.k16v8_paged_decode_append_split(self.q, self.k_new16, self.v_new16, self.kc, self.vc,
                                               self.v_scale, self.bt[r], self.seq_lens,
                                               self.max_len, self.w.sm_scale, self.chunk, self.ws,
@@ -287,6 +296,8 @@ class DecodeBench:
 
     def merge(self):
         K = self.K
+        if self.mode == "whole":  # the split kernel wrote out / lse
+            return
         if self.balanced:
             K.k16v8_merge_balanced(self.ws, self.w.num_kv_heads, self.out, self.lse)
         else:
@@ -354,7 +365,7 @@ class DecodeBench:
             lambda i: self.merge()]
         side = torch.cuda.Stream(self.dev)
         for ki, fn in enumerate(kinds):
-            if ki == 0 and self.fused:
+            if (ki == 0 and self.fused) or (ki == 2 and self.mode == "whole"):
                 outs.append(0.0)
                 continue
             g = torch.cuda.CUDAGraph()
@@ -418,7 +429,12 @@ class DecodeBench:
         d2h = o_bytes + self.lse.numel() * 4
 
         def split_launches(d):  # the step's launches up to the attention split
-            if self.mode == "balanced_fused":
+            if self.mode == "whole":
+                K.k16v8_paged_decode_append_attention(
+                    d["q"], d["k_new"], d["v_new"], self.kc, self.vc, self.v_scale, d["bt"],
+                    d["seq_lens"], self.max_len, w.sm_scale, self.chunk, self.ws, d["out"],
+                    d["lse"], self.err)
+            elif self.mode == "balanced_fused":
                 K.k16v8_paged_decode_append_balanced_split(
                     d["q"], d["k_new"], d["v_new"], self.kc, self.vc, self.v_scale, d["bt"],
                     d["seq_lens"], w.sm_scale, self.ws, d["out"], d["lse"], self.err,
@@ -441,6 +457,8 @@ class DecodeBench:
                                                self.chunk, self.ws, self.err)
 
         def merge_launch(d):
+            if self.mode == "whole":
+                return
             if self.balanced:
                 K.k16v8_merge_balanced(self.ws, w.num_kv_heads, d["out"], d["lse"])
             else:
@@ -738,6 +756,8 @@ SCHEDULE_TEXT = {
                 "separate append), LSE merge of cut segments",
     "balanced_fused": "load-balanced split with the new token's cache append folded in, LSE "
                       "merge of cut segments",
+    "whole": "one CTA per (sequence, KV head) over the whole sequence with the new token's "
+             "cache append folded in; the output written by that kernel (no merge)",
 }
 
 
@@ -1058,9 +1078,12 @@ def config_of(w, label, chunk, replicas, mode="balanced"):
     if mode in ("balanced", "balanced_fused"):
         sched = ("load-balanced split: one full wave (SMs x 4 CTAs) of equal (sequence, KV "
                  "head, page) tile ranges, LSE merge of cut segments")
+    elif mode == "whole":
+        sched = ("one CTA per (sequence, KV head) over the whole sequence, the output written "
+                 "by that kernel (no merge)")
     else:
         sched = f"split-KV chunks of {chunk} tokens, LSE merge"
-    if mode in ("fused", "balanced_fused"):
+    if mode in ("fused", "balanced_fused", "whole"):
         sched += "; the new token's cache append folded into the split kernel"
     return {"workload": f"Phi-4-shaped {label}: one layer, 40 q / 10 KV heads, head_dim 128, "
                         "16-token pages, FP16 K + E4M3 V",
@@ -1075,7 +1098,24 @@ KERNEL_NAMES = {
     "fused": ("decode_append_split", "merge_states", "decode_split_kernel<append>"),
     "balanced_fused": ("decode_append_balanced", "merge_balanced",
                        "decode_balanced_kernel<append>"),
+    "whole": ("decode_append_whole", None, "decode_split_kernel<append>"),
 }
+# launches per one-layer decode step
+LAUNCHES = {"chunked": 3, "balanced": 3, "fused": 2, "balanced_fused": 2, "whole": 1}
+
+
+def kernel_us_of(mode, append_ms, split_ms, merge_ms):
+    """Average launch duration (µs) of each kernel a step of this schedule
+    launches (no separate append for the fused schedules, no merge for
+    "whole")."""
+    split_name, merge_name, _ = KERNEL_NAMES[mode]
+    out = {}
+    if mode not in ("fused", "balanced_fused", "whole"):
+        out["kv_append"] = round(append_ms * 1e3, 2)
+    out[split_name] = round(split_ms * 1e3, 2)
+    if merge_name:
+        out[merge_name] = round(merge_ms * 1e3, 2)
+    return out
 
 
 def roofline(algo_bytes, kernel_ms, hbm_peak, peak_kind, kernel, traffic):
@@ -1098,23 +1138,23 @@ def decode_line(w, label, chunk, mode, device, steps, hbm_peak, peak_kind, workl
     import torch
     b = DecodeBench(w, device, split_chunk=chunk, mode=mode)
     ms, seg = b.run(steps, 3)
-    split_name, merge_name, kernel = KERNEL_NAMES[mode]
+    kernel = KERNEL_NAMES[mode][2]
     kvb = kv_bytes(w)
     s_ms = float(np.mean(seg[:, 1]))
     sb = kvb + w.batch * w.num_qo_heads * w.head_dim * 2
     out = {"value": round(kvb / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "us_per_layer_step": round(ms * 1e3, 2),
-           "kernel_us": {"kv_append": round(float(np.mean(seg[:, 0])) * 1e3, 2),
-                         split_name: round(s_ms * 1e3, 2),
-                         merge_name: round(float(np.mean(seg[:, 2])) * 1e3, 2)},
+           "kernel_us": kernel_us_of(mode, float(np.mean(seg[:, 0])), s_ms,
+                                     float(np.mean(seg[:, 2]))),
            "roofline": roofline(sb, s_ms, hbm_peak, peak_kind, kernel,
                                 traffic_from_profiles(workload, mode)),
            "step_frac_of_hbm_peak": round(kvb / (ms * 1e-3) / 1e9 / hbm_peak, 4),
            "step_frac_of_nominal": round(kvb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
            "config": config_of(w, label, chunk, b.R, mode)}
     if mode in ("fused", "balanced_fused"):
-        del out["kernel_us"]["kv_append"]
         out["step"] = "append fused into the split kernel, then merge (2 launches)"
+    elif mode == "whole":
+        out["step"] = "append and output in the split kernel (1 launch)"
     del b
     torch.cuda.empty_cache()
     return out
@@ -1166,7 +1206,7 @@ def measure_fullpool(args, device, rank, world):
     e2e = None
     if not args.no_e2e:
         e2e = fb.run_e2e(max(5, args.steps // 2), 3)
-    split_name, merge_name, kernel = KERNEL_NAMES[fb.schedule]
+    kernel = KERNEL_NAMES[fb.schedule][2]
     algo = fb.kv_bytes_per_layer + fb.B * 40 * 128 * 2
     units = fb.kv_bytes_per_layer * fb.layers
     per_layer = fb.step.launches_per_layer()
@@ -1176,8 +1216,7 @@ def measure_fullpool(args, device, rank, world):
         "fields": {
             "us_per_layer_step": round(ms * 1e3 / fb.layers, 2),
             "schedule_chosen": fb.schedule,
-            "kernel_us": {split_name: round(split_ms * 1e3, 2),
-                          merge_name: round(merge_ms * 1e3, 2)},
+            "kernel_us": kernel_us_of(fb.schedule, 0.0, split_ms, merge_ms),
             "roofline": roofline(algo, split_ms, hbm_peak, peak_kind, kernel,
                                  traffic_from_profiles("fullpool", fb.schedule)),
             "step_frac_of_hbm_peak": round(units / (ms * 1e-3) / 1e9 / hbm_peak, 4),
@@ -1207,18 +1246,15 @@ def measure_one_layer(args, device, rank, world):
     kvb = kv_bytes(w)
     B, hq, d = w.q.shape
     split_ms = float(np.mean(seg[:, 1]))
-    split_name, merge_name, kernel = KERNEL_NAMES[args.decode]
+    kernel = KERNEL_NAMES[args.decode][2]
     fields = {
         "us_per_layer_step": round(ms * 1e3, 2),
-        "kernel_us": {"kv_append": round(float(np.mean(seg[:, 0])) * 1e3, 2),
-                      split_name: round(split_ms * 1e3, 2),
-                      merge_name: round(float(np.mean(seg[:, 2])) * 1e3, 2)},
+        "kernel_us": kernel_us_of(args.decode, float(np.mean(seg[:, 0])), split_ms,
+                                  float(np.mean(seg[:, 2]))),
         "roofline": roofline(kvb + B * hq * d * 2, split_ms, hbm_peak, peak_kind, kernel,
                              traffic_from_profiles(args.workload, args.decode)),
-        "gpu_launches": (2 if args.decode in ("fused", "balanced_fused") else 3) * args.steps,
+        "gpu_launches": LAUNCHES[args.decode] * args.steps,
         "clocks": clk}
-    if args.decode in ("fused", "balanced_fused"):
-        del fields["kernel_us"]["kv_append"]
     res = {"ms": ms, "units": kvb, "e2e": e2e, "fields": fields,
            "config": config_of(w, label, chunk, bench.R, args.decode)}
     del bench

@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
     const int32_t *__restrict__ seq_lens, int32_t hq, int32_t hkv, int32_t num_pages,
     float sm_scale, int32_t chunk, int32_t max_chunks, float *__restrict__ part_o,
     float *__restrict__ part_lse, const __half *__restrict__ k_new,
-    const __half *__restrict__ v_new, int32_t *dev_error, int32_t test_skip_page) {
+    const __half *__restrict__ v_new, int32_t *dev_error, int32_t test_skip_page,
+    __half *__restrict__ out, float *__restrict__ lse_out) {
   using Ring = WarpRingT<kVF16 ? 2 * kVPageBytes : kVPageBytes>;
   constexpr uint32_t kVTile = kVF16 ? 2 * kVPageBytes : kVPageBytes;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -62,7 +63,17 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
     L = max(0, min(L, cap));
   }
   const int start = c * chunk;
-  if (start >= L) return;  // chunk past the end of this sequence
+  if (start >= L) {  // chunk past the end of this sequence
+    // With one chunk the CTA writes the final rows (out != null): an empty
+    // sequence gets zero rows and LSE -inf, as the merge would give.
+    if (out) {
+      const int h = threadIdx.x >> 5;
+      const int64_t orow = static_cast<int64_t>(b) * hq + g * kGroup + h;
+      *reinterpret_cast<uint2 *>(out + orow * kHeadDim + lane * 4) = make_uint2(0u, 0u);
+      if (lane == 0 && lse_out) lse_out[orow] = -INFINITY;
+    }
+    return;
+  }
   const int n_tok = min(chunk, L - start);
   const int n_pages = (n_tok + kPage - 1) / kPage;
 
@@ -206,8 +217,21 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
       res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       lse = (M + lg2(Ls)) * kLn2;
     }
-    *reinterpret_cast<float4 *>(part_o + row * kHeadDim + d4) = res;
-    if ((threadIdx.x & 31) == 0) part_lse[row] = lse;
+    if (out) {
+      // one chunk: this is the final row (what the merge of a single partial
+      // gives: the same values, rounded to fp16)
+      const int64_t orow = static_cast<int64_t>(b) * hq + g * kGroup + h;
+      uint2 o2;
+      o2.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(res.x))) |
+             (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(res.y))) << 16);
+      o2.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(res.z))) |
+             (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(res.w))) << 16);
+      *reinterpret_cast<uint2 *>(out + orow * kHeadDim + d4) = o2;
+      if ((threadIdx.x & 31) == 0 && lse_out) lse_out[orow] = lse;
+    } else {
+      *reinterpret_cast<float4 *>(part_o + row * kHeadDim + d4) = res;
+      if ((threadIdx.x & 31) == 0) part_lse[row] = lse;
+    }
   }
 }
 
@@ -356,7 +380,8 @@ static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v
                             int32_t num_kv_heads, int32_t head_dim, int32_t num_pages,
                             float sm_scale, int32_t split_chunk, void *workspace,
                             size_t workspace_bytes, const void *k_new, const void *v_new,
-                            int32_t *dev_error, void *stream, int32_t test_skip_page = -1) {
+                            int32_t *dev_error, void *stream, int32_t test_skip_page = -1,
+                            void *out = nullptr, float *lse = nullptr) {
   int32_t st = check_attention_shape(num_qo_heads, num_kv_heads, head_dim);
   if (st != K16V8_OK) return st;
   if (batch < 0 || max_seq_len < 0 || num_pages <= 0 || max_pages_per_seq < 0)
@@ -380,6 +405,8 @@ static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v
       !k16v8_aligned(seq_lens, 4) || !k16v8_aligned(v_scale, 4))
     return K16V8_ERR_INVALID_ARG;
   if (max_seq_len == 0) return K16V8_OK;  // every sequence empty: nothing to read
+  if (w.chunks == 1 && out && (!k16v8_aligned(out, 8) || (lse && !k16v8_aligned(lse, 4))))
+    return K16V8_ERR_INVALID_ARG;
   const size_t smem = decode_smem_bytes(split_chunk, kVF16);
   st = set_smem_attr<kAppend, kVF16>(smem);
   if (st != K16V8_OK) return st;
@@ -392,7 +419,17 @@ static int32_t launch_split(const void *q, const void *k_cache, const uint8_t *v
       static_cast<__half *>(const_cast<void *>(k_cache)), const_cast<uint8_t *>(v_cache), v_scale,
       block_table, max_pages_per_seq, seq_lens, num_qo_heads, num_kv_heads, num_pages, sm_scale,
       split_chunk, w.chunks, po, pl, static_cast<const __half *>(k_new),
-      static_cast<const __half *>(v_new), dev_error, test_skip_page);
+      static_cast<const __half *>(v_new), dev_error, test_skip_page,
+      w.chunks == 1 ? static_cast<__half *>(out) : nullptr, w.chunks == 1 ? lse : nullptr);
+}
+
+// A combined call whose lengths fit one chunk launches only the split
+// kernel, which then writes the output rows itself (no partials, no merge).
+static bool single_chunk(int32_t batch, int32_t hq, int32_t d, int32_t max_seq_len,
+                         int32_t split_chunk) {
+  WsLayout w;
+  return batch > 0 && max_seq_len > 0 &&
+         ws_layout(batch, hq, d, max_seq_len, split_chunk, &w) && w.chunks == 1;
 }
 
 extern "C" int32_t k16v8_paged_decode_split(
@@ -474,6 +511,12 @@ extern "C" int32_t k16v8_paged_decode_attention(
     int32_t head_dim, int32_t num_pages, float sm_scale, int32_t split_chunk, void *workspace,
     size_t workspace_bytes, void *out, float *lse, int32_t *dev_error, void *stream) {
   if (batch > 0 && !out) return K16V8_ERR_INVALID_ARG;
+  if (single_chunk(batch, num_qo_heads, head_dim, max_seq_len, split_chunk))
+    return launch_split<false>(q, k_cache, v_cache, v_scale, block_table, max_pages_per_seq,
+                               seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads,
+                               head_dim, num_pages, sm_scale, split_chunk, workspace,
+                               workspace_bytes, nullptr, nullptr, dev_error, stream, -1, out,
+                               lse);
   int32_t st = k16v8_paged_decode_split(q, k_cache, v_cache, v_scale, block_table,
                                         max_pages_per_seq, seq_lens, max_seq_len, batch,
                                         num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale,
@@ -496,6 +539,11 @@ extern "C" int32_t k16v8_paged_decode_append_attention(
     int32_t split_chunk, void *workspace, size_t workspace_bytes, void *out, float *lse,
     int32_t *dev_error, void *stream) {
   if (batch > 0 && !out) return K16V8_ERR_INVALID_ARG;
+  if (single_chunk(batch, num_qo_heads, head_dim, max_seq_len, split_chunk))
+    return launch_split<true>(q, k_cache, v_cache, v_scale, block_table, max_pages_per_seq,
+                              seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim,
+                              num_pages, sm_scale, split_chunk, workspace, workspace_bytes, k_new,
+                              v_new, dev_error, stream, -1, out, lse);
   int32_t st = k16v8_paged_decode_append_split(
       q, k_new, v_new, k_cache, v_cache, v_scale, block_table, max_pages_per_seq, seq_lens,
       max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim, num_pages, sm_scale, split_chunk,
@@ -517,6 +565,12 @@ extern "C" int32_t k16v8_paged_decode_attention_v16(
     float sm_scale, int32_t split_chunk, void *workspace, size_t workspace_bytes, void *out,
     float *lse, int32_t *dev_error, void *stream) {
   if (batch > 0 && !out) return K16V8_ERR_INVALID_ARG;
+  if (single_chunk(batch, num_qo_heads, head_dim, max_seq_len, split_chunk))
+    return launch_split<false, true>(
+        q, k_cache, static_cast<const uint8_t *>(v_cache16), nullptr, block_table,
+        max_pages_per_seq, seq_lens, max_seq_len, batch, num_qo_heads, num_kv_heads, head_dim,
+        num_pages, sm_scale, split_chunk, workspace, workspace_bytes, nullptr, nullptr, dev_error,
+        stream, -1, out, lse);
   int32_t st = k16v8_paged_decode_split_v16(q, k_cache, v_cache16, block_table,
                                             max_pages_per_seq, seq_lens, max_seq_len, batch,
                                             num_qo_heads, num_kv_heads, head_dim, num_pages,

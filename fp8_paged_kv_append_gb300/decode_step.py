@@ -66,7 +66,10 @@ class MultiLayerDecode:
     and its merge; "balanced_fused": the same with each layer's append done
     by the split kernel itself (2 launches per layer instead of 3; the slot
     of the new token is then the one the block table gives for position
-    seq_len - 1, which `slots` must agree with).  The block table and lengths
+    seq_len - 1, which `slots` must agree with); "whole": one CTA per
+    (sequence, KV head) over the whole sequence with the append folded in,
+    the output written by that kernel (1 launch per layer, no merge; needs
+    max_seq_len <= 8192).  The block table and lengths
     are written only by host copies, never by the kernel before the
     attention, so the balanced split may read them ahead of its wait on that
     kernel.  "auto" picks "balanced_fused" or "fused" by choose_schedule
@@ -91,8 +94,12 @@ class MultiLayerDecode:
         if schedule == "auto":  # by the lengths of this batch (read once, here)
             schedule = choose_schedule(seq_lens.detach().cpu().tolist(), k_caches[0].shape[1],
                                        torch.cuda.get_device_properties(dev).multi_processor_count)
-        if schedule not in ("chunked", "fused", "balanced", "balanced_fused"):
+        if schedule not in ("chunked", "fused", "balanced", "balanced_fused", "whole"):
             raise ValueError(f"unknown schedule {schedule!r}")
+        if schedule == "whole":  # one chunk covering the longest sequence
+            self.chunk = max(16, -(-self.max_seq_len // 16) * 16)
+            if self.chunk > K.MAX_SPLIT_CHUNK:
+                raise ValueError(f"schedule 'whole' needs max_seq_len <= {K.MAX_SPLIT_CHUNK}")
         self.schedule = schedule
         if schedule in ("balanced", "balanced_fused"):
             n = K.k16v8_decode_balanced_workspace_size(self.batch, self.hq, self.d)
@@ -115,7 +122,12 @@ class MultiLayerDecode:
     def split(self, li, q, k_new, v_new, out, lse=None, append=True):
         """Layer li's launches up to the attention split (the separate append
         first, unless the split kernel does it or append is False)."""
-        if self.schedule == "balanced_fused":
+        if self.schedule == "whole":
+            K.k16v8_paged_decode_append_attention(
+                q, k_new, v_new, self.k_caches[li], self.v_caches[li], self.v_scales[li],
+                self.block_table, self.seq_lens, self.max_seq_len, self.sm_scale, self.chunk,
+                self.workspace, out, lse, self.dev_error)
+        elif self.schedule == "balanced_fused":
             K.k16v8_paged_decode_append_balanced_split(
                 q, k_new, v_new, self.k_caches[li], self.v_caches[li], self.v_scales[li],
                 self.block_table, self.seq_lens, self.sm_scale, self.workspace, out, lse,
@@ -142,7 +154,10 @@ class MultiLayerDecode:
                                            self.workspace, self.dev_error)
 
     def merge(self, li, out, lse=None):
-        """Layer li's merge of the split partials into out / lse."""
+        """Layer li's merge of the split partials into out / lse (none for
+        "whole", whose split kernel writes them)."""
+        if self.schedule == "whole":
+            return
         if self.schedule in ("balanced", "balanced_fused"):
             K.k16v8_merge_balanced(self.workspace, self.hkv, out, lse)
         else:
@@ -150,7 +165,10 @@ class MultiLayerDecode:
                                  out, lse)
 
     def launches_per_layer(self) -> int:
-        """Launches per layer: 2 when the append runs inside the split."""
+        """Launches per layer: 2 when the append runs inside the split, 1 when
+        the split also writes the output."""
+        if self.schedule == "whole":
+            return 1
         return 2 if self.schedule in ("fused", "balanced_fused") else 3
 
     def step(self, qs, k_news, v_news, outs, lses=None):

@@ -30,6 +30,7 @@ DECODE_METADATA_READY = 1
 DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8, 16
 PAGE_SIZE = 16
 HEAD_DIM = 128
+MAX_SPLIT_CHUNK = 8192  # K16V8_MAX_SPLIT_CHUNK
 
 # Every symbol include/k16v8.h declares, with its ctypes signature.
 _P = ctypes.c_void_p

@@ -176,7 +176,12 @@ int32_t k16v8_merge_states(const float *partial_o, const float *partial_lse,
  * paged_decode_attention -- k16v8_paged_decode_split followed by
  * k16v8_merge_states on the same stream, writing fp16 out
  * [batch][num_qo_heads][head_dim] and fp32 lse [batch][num_qo_heads] (lse may
- * be NULL).  Arguments as for the two calls.
+ * be NULL).  Arguments as for the two calls.  When max_seq_len <= split_chunk
+ * (one chunk per sequence) only the split kernel is launched: each CTA
+ * writes its rows of out / lse directly (zero rows and -inf for an empty
+ * sequence), bit-equal to the merge of the single partial, and the
+ * workspace is not written (it must still be given and large enough).
+ * out must be 8-byte aligned.
  */
 int32_t k16v8_paged_decode_attention(const void *q, const void *k_cache,
                                      const uint8_t *v_cache, const float *v_scale,
@@ -294,8 +299,9 @@ int32_t k16v8_paged_decode_append_attention_balanced(
  *                 16-B aligned: the K and V of each sequence's new token
  *   seq_lens      lengths INCLUDING the new token (a sequence with L = 0 has
  *                 no new token and is skipped)
- * Other arguments as for k16v8_paged_decode_split / _attention.  The cache
- * row is written with the same rounding as k16v8_kv_append.
+ * Other arguments as for k16v8_paged_decode_split / _attention (including
+ * the one-chunk case of _attention: a single launch that writes out / lse).
+ * The cache row is written with the same rounding as k16v8_kv_append.
  */
 int32_t k16v8_paged_decode_append_split(const void *q, const void *k_new, const void *v_new,
                                         void *k_cache, uint8_t *v_cache, const float *v_scale,

@@ -38,6 +38,20 @@ def run_decode(K, w, kc, vc, chunk, err=None, max_seq_len=None, block_table=None
     return out, lse, po, pl
 
 
+def split_then_merge(K, w, kc, vc, chunk, max_len):
+    """The same call as two launches: the split's partials, then the merge."""
+    B, hq, d = w.q.shape
+    ws = torch.zeros(K.k16v8_decode_workspace_size(B, hq, d, max_len, chunk),
+                     dtype=torch.uint8, device=dev())
+    K.k16v8_paged_decode_split(to_dev(w.q), kc, vc, to_dev(w.v_scale), to_dev(w.block_table),
+                               to_dev(w.seq_lens), max_len, w.sm_scale, chunk, ws)
+    po, pl = K.workspace_views(ws, B, hq, d, max_len, chunk)
+    out = torch.empty((B, hq, d), dtype=torch.float16, device=dev())
+    lse = torch.empty((B, hq), dtype=torch.float32, device=dev())
+    K.k16v8_merge_states(po, pl, to_dev(w.seq_lens), chunk, out, lse)
+    return out, lse, po, pl
+
+
 def compare_workload(K, w, chunk, check_partials=True):
     err = torch.zeros(1, dtype=torch.int32, device=dev())
     kc, vc = gpu_cache(w, K, err)
@@ -49,6 +63,15 @@ def compare_workload(K, w, chunk, check_partials=True):
     ref = oracle.paged_decode(w.q, okc, ovc, w.v_scale, w.block_table, w.seq_lens,
                               w.sm_scale, split_chunk=chunk if check_partials else 0)
     check_close(out.float().cpu().numpy(), ref["out"], lse.cpu().numpy(), ref["lse"])
+    max_len = int(w.seq_lens.max(initial=0))
+    if check_partials and max_len <= chunk:
+        # One chunk: the split kernel wrote the rows itself and no partials
+        # (the workspace stays as allocated, zero).  The same call as split +
+        # merge gives the same bits, and its partials are checked below.
+        assert not torch.any(po) and not torch.any(pl)
+        o2, l2, po, pl = split_then_merge(K, w, kc, vc, chunk, max_len)
+        assert torch.equal(out.view(torch.int16), o2.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), l2.view(torch.int32))
     if check_partials:
         nc = -(-w.seq_lens // chunk)
         po_h, pl_h = po.cpu().numpy(), pl.cpu().numpy()
@@ -90,6 +113,19 @@ def test_decode_ragged_edges(K):
     l = lse.cpu().numpy()
     assert np.all(o[0] == 0) and np.all(np.isneginf(l[0]))
     check_close(o, ref["out"], l, ref["lse"])
+
+
+@pytest.mark.parametrize("maker,chunk", [
+    (lambda: workloads.make_decode("ragged", 33, [0, 1, 15, 16, 17, 511, 512, 513, 1000],
+                                   num_qo_heads=8, num_kv_heads=2), 1008),
+    (workloads.decode_1k_b32, 1152),
+    (workloads.decode_1k_b32, 8192)])
+def test_decode_single_chunk_writes_output_directly(K, maker, chunk):
+    """Lengths that fit one chunk: the combined call launches the split kernel
+    alone, which writes out / lse (an empty sequence: 0 and -inf), bit-equal
+    to the split + merge of its one partial and within tolerance of the
+    oracle."""
+    compare_workload(K, maker(), chunk)
 
 
 def test_decode_uniform_keys_gives_mean_of_values(K):

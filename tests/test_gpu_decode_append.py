@@ -81,6 +81,50 @@ def test_fused_append_equals_separate_append(K):
     assert torch.equal(o1, o2)
 
 
+@pytest.mark.parametrize("maker", [
+    lambda: workloads.make_decode("ragged with empty", 53, [1, 0, 16, 17, 200, 0, 513, 1000],
+                                  num_qo_heads=8, num_kv_heads=2),
+    workloads.decode_1k_b32])
+def test_fused_append_single_chunk_writes_output_directly(K, maker):
+    """Lengths that fit one chunk: the fused split writes the cache row and the
+    output itself (one launch).  Cache bytes and outputs equal the fused
+    split + merge bit for bit; outputs match the oracle."""
+    w = maker()
+    w.v_tok = w.v_tok.astype(np.float16)
+    kc, vc, okc, ovc = cache_without_new_tokens(w, K)
+    kc2, vc2 = kc.clone(), vc.clone()
+    B, hq, d = w.q.shape
+    L = int(w.seq_lens.max())
+    has_new = w.new_rows >= 0
+    nr = np.where(has_new, w.new_rows, 0)  # rows of empty sequences are never read
+    chunk = -(-L // 16) * 16
+    ws = torch.zeros(K.k16v8_decode_workspace_size(B, hq, d, L, chunk), dtype=torch.uint8,
+                     device=dev())
+    ws2 = torch.zeros_like(ws)
+    o1 = torch.empty((B, hq, d), dtype=torch.float16, device=dev())
+    l1 = torch.empty((B, hq), dtype=torch.float32, device=dev())
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    kn = to_dev(np.ascontiguousarray(w.k_tok[nr]))
+    vn = to_dev(np.ascontiguousarray(w.v_tok[nr]))
+    args = (to_dev(w.v_scale), to_dev(w.block_table), to_dev(w.seq_lens), L, w.sm_scale, chunk)
+    K.k16v8_paged_decode_append_attention(to_dev(w.q), kn, vn, kc, vc, *args, ws, o1, l1, err)
+    assert not torch.any(ws)  # no partials written
+    K.k16v8_paged_decode_append_split(to_dev(w.q), kn, vn, kc2, vc2, *args, ws2, err)
+    po, pl = K.workspace_views(ws2, B, hq, d, L, chunk)
+    K.k16v8_merge_states(po, pl, to_dev(w.seq_lens), chunk, o2, l2)
+    assert K.k16v8_read_device_error(err) == 0
+    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16)) and torch.equal(vc, vc2)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+    sel = w.new_rows[has_new]
+    oracle.kv_append(w.k_tok[sel], w.v_tok[sel], w.slot_mapping[sel], w.v_scale, okc, ovc)
+    hk, hv = host_bits(kc, vc)
+    assert np.array_equal(hk, okc.view(np.uint16)) and np.array_equal(hv, ovc)
+    ref = oracle.paged_decode(w.q, okc, ovc, w.v_scale, w.block_table, w.seq_lens, w.sm_scale)
+    check_close(o1.float().cpu().numpy(), ref["out"], l1.cpu().numpy(), ref["lse"])
+
+
 @pytest.mark.parametrize("maker,flags", [
     (lambda: workloads.make_decode("ragged with empty", 52, [1, 0, 16, 17, 200, 0, 513, 1000],
                                    num_qo_heads=8, num_kv_heads=2), 0),

@@ -99,12 +99,13 @@ def test_scale_validation_rejects_bad_scale(setup):
         validate_scales(bad)
 
 
-@pytest.mark.parametrize("schedule", ["balanced", "balanced_fused", "fused", "auto"])
+@pytest.mark.parametrize("schedule", ["balanced", "balanced_fused", "fused", "whole", "auto"])
 def test_fullpool_other_schedules_match_oracle(setup, schedule):
     """The same 40-layer step on the load-balanced split (block table and
     lengths read ahead of the wait on the preceding kernel), with and without
-    the append folded in, the chunked split with the append folded in, and
-    the automatic choice (captured graph each): every sequence of layers 0,
+    the append folded in, the chunked split with the append folded in, one
+    CTA per (sequence, KV head) writing the output itself (one launch per
+    layer), and the automatic choice (captured graph each): every sequence of layers 0,
     17 and 39 against the oracle.  Folded-in appends write the same bytes to the
     same slots as the separate append."""
     from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
