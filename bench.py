@@ -1043,24 +1043,84 @@ def oracle_cache_for(w):
     return okc, ovc
 
 
-def run_cpu_baseline(w, chunk, sample, desc, budget_s=12.0):
+def run_cpu_baseline(w, chunk, sample, desc, budget_s=12.0, single_budget_s=None):
     """Time the oracle, as it stands, on a bounded sample of the workload:
-    decode passes over sequences `sample` of w until `budget_s` has passed."""
+    decode passes over sequences `sample` of w until `budget_s` has passed,
+    on every host core; then (single_budget_s, default a quarter of that) the
+    same passes on one thread."""
     ncores = os.cpu_count() or 1
     okc, ovc = oracle_cache_for(w)
-    t0 = time.perf_counter()
-    bytes_done = 0
-    passes = 0
-    while True:
-        bytes_done += oracle_decode_pass(w, okc, ovc, chunk, sample, ncores)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or passes >= 5000:
-            break
-    return {"value": round(bytes_done / el / 1e9, 4), "unit": "GB/s", "cores": ncores,
-            "kind": "oracle",
+
+    def timed(nthreads, budget):
+        t0 = time.perf_counter()
+        bytes_done = passes = 0
+        while True:
+            bytes_done += oracle_decode_pass(w, okc, ovc, chunk, sample, nthreads)
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= budget or passes >= 5000:
+                return bytes_done / el / 1e9, passes, el
+
+    v, passes, el = timed(ncores, budget_s)
+    v1, passes1, el1 = timed(1, budget_s / 4 if single_budget_s is None else single_budget_s)
+    return {"value": round(v, 4), "unit": "GB/s", "cores": ncores, "kind": "oracle",
             "sample": f"{passes} oracle decode steps (append + split partials + merge) over "
-                      f"{desc}, {el:.1f} s wall"}
+                      f"{desc}, {el:.1f} s wall",
+            "single_thread_value": round(v1, 4),
+            "single_thread_sample": f"{passes1} of the same steps on one thread, {el1:.1f} s"}
+
+
+def prefill_cpu_baseline(p, row_stride=64, budget_s=4.0):
+    """The oracle's prefill attention and cache write, as they stand, on a
+    bounded sample of a prefill workload: the cache write of every prompt
+    token (GB/s against kv_append's 8,960 B per token), then the causal
+    attention of every row_stride-th query row of the first call (TFLOP/s
+    against 4 D Hq (position + 1) flops per row), repeated for about
+    budget_s on all host cores and once on one thread."""
+    import oracle
+    ncores = os.cpu_count() or 1
+    okc = np.zeros((p.num_pages, p.num_kv_heads, 16, p.head_dim), np.float16)
+    ovc = np.zeros((p.num_pages, p.num_kv_heads, 16, p.head_dim), np.uint8)
+    t0 = time.perf_counter()
+    oracle.kv_append(p.k_tok, p.v_tok, p.slot_mapping, p.v_scale, okc, ovc)
+    t_app = time.perf_counter() - t0
+    call = p.calls[0]
+    q = np.ascontiguousarray(p.q[call.rows])
+    rows = np.arange(0, len(call.rows), row_stride, dtype=np.int64)
+    # absolute position of each sampled query row
+    seq_of = np.searchsorted(call.qo_indptr, rows, side="right") - 1
+    pos = (call.seq_lens[seq_of].astype(np.int64) - (call.qo_indptr[seq_of + 1]
+           - call.qo_indptr[seq_of]) + (rows - call.qo_indptr[seq_of]))
+
+    def flops_of(r):
+        return float(4 * p.head_dim * p.num_qo_heads * int((pos[r] + 1).sum()))
+
+    def timed(sel, nthreads, budget):
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            oracle.paged_prefill(q, call.qo_indptr, okc, ovc, p.v_scale, call.block_table,
+                                 call.seq_lens, p.sm_scale, rows=rows[sel], nthreads=nthreads)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget or n >= 1000:
+                return flops_of(sel) * n / el / 1e12, n, el
+
+    every = np.arange(len(rows))
+    v, n, el = timed(every, ncores, budget_s)
+    one = every[::4]  # the single-thread pass takes a quarter of the rows
+    v1, n1, el1 = timed(one, 1, 0.0)
+    return {"value": round(v, 6), "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
+            "sample": f"{n} oracle passes over every {row_stride}th query row of the first call "
+                      f"({len(rows)} rows, {flops_of(every) / 1e9:.2f} GFLOP each), {el:.1f} s "
+                      "wall",
+            "single_thread_value": round(v1, 6),
+            "single_thread_sample": f"{n1} pass over every {4 * row_stride}th row on one "
+                                    f"thread, {el1:.1f} s",
+            "kv_append": {"value": round(kv_append_bytes(p) / t_app / 1e9, 4), "unit": "GB/s",
+                          "threads": 1,
+                          "sample": f"the cache write of all {p.q.shape[0]} prompt tokens, "
+                                    f"{t_app:.2f} s"}}
 
 
 # ---- decode lines of one layer ------------------------------------------------------
@@ -1287,6 +1347,8 @@ def extra_lines(args, device):
                                "prefill_8x1024"),
         "1x8192_in_8_chunks": prefill_line(workloads.prefill_1x8k(), device, 5, 2, tpeak,
                                            hbm_peak)}
+    if not args.no_cpu:
+        extra["prefill"]["8x1024"]["cpu_baseline"] = prefill_cpu_baseline(workloads.prefill_8x1k())
     for name, (wf, lf, cf) in (("decode_1k_b32", (w1, l1, c1)), ("decode_8k_b16", (w8, l8, c8))):
         torch.cuda.empty_cache()
         ctl = fp16_control_line(wf, device, cf, n2, 3, hbm_peak)
