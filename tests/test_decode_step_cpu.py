@@ -30,3 +30,29 @@ def test_choose_schedule_follows_tiles_per_cta():
     # the boundary: exactly 160 tiles per CTA, then one page more
     assert choose_schedule([160 * 16 * 608 // 10], 10, 152) == "balanced_fused"
     assert choose_schedule([160 * 16 * 608 // 10 + 16], 10, 152) == "fused"
+
+
+def _cpu_step(max_seq_len, schedule):
+    from fp8_paged_kv_append_gb300.decode_step import MultiLayerDecode
+    P, hkv = 8, 2
+    kc = [torch.zeros((P, hkv, 16, 128), dtype=torch.float16)]
+    vc = [torch.zeros((P, hkv, 16, 128), dtype=torch.uint8)]
+    vs = [torch.ones(hkv)]
+    bt = torch.zeros((2, 4), dtype=torch.int32)
+    lens = torch.tensor([5, 9], dtype=torch.int32)
+    slots = torch.zeros(2, dtype=torch.int64)
+    return MultiLayerDecode(kc, vc, vs, bt, lens, slots, max_seq_len, 4 * hkv,
+                            schedule=schedule)
+
+
+def test_whole_schedule_is_one_launch_per_layer():
+    """One CTA per (sequence, KV head) over the whole sequence: the split
+    kernel writes the output, so a layer is one launch and the chunk covers
+    the longest sequence."""
+    step = _cpu_step(1000, "whole")
+    assert step.launches_per_layer() == 1 and step.chunk == 1008
+
+
+def test_whole_schedule_refuses_sequences_beyond_the_largest_chunk():
+    with pytest.raises(ValueError, match="whole"):
+        _cpu_step(9000, "whole")
