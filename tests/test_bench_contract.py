@@ -66,3 +66,22 @@ def test_replicas_cover_four_l2():
         w, _, _ = bench.make_workload(name)
         pool = w.num_pages * w.num_kv_heads * 16 * w.head_dim * 3
         assert bench.replicas_for(w) * pool >= 4 * bench.L2_BYTES
+
+
+def test_oracle_baselines_report_all_cores_and_one_thread():
+    """The host baselines of the default line: the oracle's decode steps on
+    every core and on one thread, and the oracle's prefill attention and
+    cache write beside the prefill line (tiny workloads here)."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from fp8_paged_kv_append_gb300 import workloads
+    w = workloads.make_decode("tiny", 3, [37, 200], num_qo_heads=8, num_kv_heads=2)
+    d = bench.run_cpu_baseline(w, 64, np.arange(w.batch), "tiny", budget_s=0.2)
+    assert d["kind"] == "oracle" and d["unit"] == "GB/s" and d["cores"] >= 1
+    assert d["value"] > 0 and d["single_thread_value"] > 0
+    p = workloads.make_prefill("tiny", 4, [70, 33], chunk=64, num_qo_heads=8, num_kv_heads=2)
+    d = bench.prefill_cpu_baseline(p, row_stride=4, budget_s=0.2)
+    assert d["kind"] == "oracle" and d["unit"] == "TFLOP/s" and d["cores"] >= 1
+    assert d["value"] > 0 and d["single_thread_value"] > 0
+    assert d["kv_append"]["unit"] == "GB/s" and d["kv_append"]["value"] > 0
