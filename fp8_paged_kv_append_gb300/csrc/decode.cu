@@ -236,9 +236,12 @@ __global__ void __launch_bounds__(kWarps * 32, kVF16 ? 3 : kMinBlocks) decode_sp
 }
 
 // One warp per (sequence, query head); lane owns 4 dims.  The live chunks'
-// LSEs are loaded lane-parallel; partial rows are read 4 at a time so their
-// loads are in flight together.
-__global__ void __launch_bounds__(128, 8) merge_states_kernel(
+// LSEs are loaded lane-parallel.  A row of up to kMergeOneRound chunks (a
+// whole 8192-token sequence at the default 512-token chunk) has every
+// partial row in flight in one round of loads; longer rows are read 4
+// chunks at a time.  Either way the sums run in chunk order.
+constexpr int kMergeOneRound = 16;
+__global__ void __launch_bounds__(128, 5) merge_states_kernel(
     const float *__restrict__ part_o, const float *__restrict__ part_lse, int32_t rows,
     int32_t hq, int32_t max_chunks, const int32_t *__restrict__ seq_lens, int32_t chunk,
     __half *__restrict__ out, float *__restrict__ lse_out) {
@@ -253,13 +256,32 @@ __global__ void __launch_bounds__(128, 8) merge_states_kernel(
   const int nc = (L + chunk - 1) / chunk;
   const float *pl = part_lse + static_cast<int64_t>(wid) * max_chunks;
   const float *po = part_o + static_cast<int64_t>(wid) * max_chunks * kHeadDim + lane * 4;
-  float M = -INFINITY;
-  for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldg(pl + c));
+  const float lc = lane < nc ? __ldg(pl + lane) : -INFINITY;  // LSE of chunk `lane`
+  float M = lc;
+  for (int c = lane + 32; c < nc; c += 32) M = fmaxf(M, __ldg(pl + c));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
   float S = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
+  if (M != -INFINITY && nc <= kMergeOneRound) {
+    float4 oc[kMergeOneRound];
+#pragma unroll
+    for (int c = 0; c < kMergeOneRound; ++c)
+      oc[c] = c < nc ? __ldg(reinterpret_cast<const float4 *>(po + static_cast<int64_t>(c) * kHeadDim))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kMergeOneRound; ++c) {
+      const float wl = __shfl_sync(kFull, lc, c);
+      if (c < nc) {
+        const float wu = ex2((wl - M) * kLog2e);
+        S += wu;
+        acc.x = fmaf(wu, oc[c].x, acc.x);
+        acc.y = fmaf(wu, oc[c].y, acc.y);
+        acc.z = fmaf(wu, oc[c].z, acc.z);
+        acc.w = fmaf(wu, oc[c].w, acc.w);
+      }
+    }
+  } else if (M != -INFINITY) {
     int c = 0;
     for (; c + 4 <= nc; c += 4) {
       float4 oc[4];
